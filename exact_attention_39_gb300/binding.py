@@ -1,0 +1,153 @@
+"""ctypes binding of the C ABI in include/fa.h.
+
+Argument marshalling only: every step of the attention forward runs in the
+CUDA kernel behind ``fa_fwd``.  PyTorch supplies device memory and streams.
+There is no fallback: if the shared library is missing or the call fails,
+these functions raise.
+"""
+import ctypes
+import math
+import os
+
+import torch
+
+from . import _build
+
+FA_OK = 0
+FA_ERR_NULL = 1
+FA_ERR_SHAPE = 2
+FA_ERR_HEADDIM = 3
+FA_ERR_DTYPE = 4
+FA_ERR_ALIGN = 5
+FA_ERR_SCALE = 6
+FA_ERR_CUDA = 7
+FA_ERR_DEVICE_TIMEOUT = 8
+FA_FP16 = 0
+FA_BF16 = 1
+
+EXPORTED = ("fa_fwd", "fa_status_string", "fa_last_device_error", "fa_version")
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__("%s (status %d)" % (msg, status))
+        self.status = status
+
+
+def load_library(path=None):
+    """Load libfa_sm103.so (built in-tree by ``_build.build``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(
+            "%s is not built; run `python -c \"import __graft_entry__ as g; "
+            "g.build()\"` first (there is no CPU fallback)" % path)
+    lib = ctypes.CDLL(path)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_last_device_error.argtypes = [vp]
+    lib.fa_last_device_error.restype = i
+    lib.fa_version.argtypes = []
+    lib.fa_version.restype = i
+    if path == _build.LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def status_string(status):
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def _check(status):
+    if status != FA_OK:
+        raise FaError(status, status_string(status))
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def fa_fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, causal,
+               scale, dtype_code, stream_handle):
+    """The C call with plain integers; returns the status code."""
+    return load_library().fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B),
+                                 int(H), int(N), int(d), int(bool(causal)),
+                                 float(scale), int(dtype_code), stream_handle)
+
+
+def _dtype_code(t):
+    if t.dtype == torch.float16:
+        return FA_FP16
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    raise TypeError("q, k, v must be float16 or bfloat16, got %s" % t.dtype)
+
+
+def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None):
+    """Attention forward on CUDA tensors ``q, k, v`` of shape [B, H, N, d].
+
+    Returns ``(o, lse)``: ``o`` like ``q``; ``lse`` [B, H, N] float32.
+    ``scale`` defaults to 1/sqrt(d).  The kernel is enqueued on ``stream``
+    (default: the current torch stream); nothing is synchronised.
+    """
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must all be [B, H, N, d] with equal shapes")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    code = _dtype_code(q)
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor like q")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    with torch.cuda.device(q.device):
+        _check(fa_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                          out.data_ptr(), lse.data_ptr(), B, H, N, d, causal,
+                          scale, code, _stream_handle(stream)))
+    return out, lse
+
+
+def fwd_host(q_h, k_h, v_h, q_d, k_d, v_d, o_d, lse_d, o_h, lse_h,
+             causal=False, scale=None, stream=None):
+    """End-to-end call from host memory: copy q, k, v (pinned host tensors)
+    into the device buffers, run ``fa_fwd``, copy O and LSE back into the
+    pinned host tensors ``o_h``/``lse_h``.  All copies and the kernel are
+    enqueued on one stream; the call returns after synchronising it."""
+    stream = stream or torch.cuda.current_stream()
+    with torch.cuda.stream(stream):
+        q_d.copy_(q_h, non_blocking=True)
+        k_d.copy_(k_h, non_blocking=True)
+        v_d.copy_(v_h, non_blocking=True)
+        fwd(q_d, k_d, v_d, causal=causal, scale=scale, out=o_d, lse=lse_d,
+            stream=stream)
+        o_h.copy_(o_d, non_blocking=True)
+        lse_h.copy_(lse_d, non_blocking=True)
+    stream.synchronize()
+    return o_h, lse_h
+
+
+def last_device_error(stream=None):
+    """Synchronise and return the device status (FA_OK or an error code)."""
+    return load_library().fa_last_device_error(_stream_handle(stream))
+
+
+def version():
+    return load_library().fa_version()

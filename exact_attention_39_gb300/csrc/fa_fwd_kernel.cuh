@@ -1,0 +1,456 @@
+// fa_fwd_kernel.cuh -- the attention forward kernel for sm_103a.
+//
+// What it computes: O = softmax(scale * Q K^T [+ causal mask]) V and the
+// per-row logsumexp, for one (batch, head) problem per group of CTAs.  The
+// pages describe the method as splitting the computation into blocks that
+// fit in on-chip memory so the attention matrix never goes to HBM
+// (zzycbzc.com/news/393333, section "FlashAttention的技术革命"; the
+// "0 MB (recompute)" column of the benchmarks page's Flash Attention 2
+// memory table).  Keeping only a running row maximum and a running row sum
+// (the online softmax) is what makes one pass over the key blocks exact.
+//
+// Shape of one CTA (a "work unit" = 256 query rows of one head):
+//   warps 0-3  softmax warpgroup for query tile 0 (rows q0 .. q0+127)
+//   warps 4-7  softmax warpgroup for query tile 1 (rows q0+128 .. q0+255)
+//              thread t of a warpgroup owns query row t = TMEM lane t
+//   warp  8    TMA producer: Q tiles once, then K/V blocks into a ring
+//   warp  9    TMEM allocator and tcgen05 MMA issuer (one thread)
+//
+// Per key block j the MMA thread issues, in this order,
+//   PV_0(j-1)... i.e.   O_0 += P_0 V_j ; S_0 = Q_0 K_{j+1}^T ;
+//                       O_1 += P_1 V_j ; S_1 = Q_1 K_{j+1}^T
+// so that while one softmax warpgroup works on its scores the tensor core
+// works for the other (ping-pong).  A commit after S_i(j+1) tracks every
+// earlier MMA of the thread, so when a softmax warpgroup sees S_i(j+1) ready
+// it also knows that O_i += P_i V_j has finished: it may then rescale O_i and
+// overwrite P_i.
+//
+// TMEM (512 columns, fp32 cells, 128 lanes):
+//   S_i  at columns i*128 .. i*128+127   (scores of tile i, one row per lane)
+//   O_i  at columns 256 + i*D           (output accumulator of tile i)
+//   P_i  (16-bit probabilities, two per cell) at 384 + i*64 for D = 64; for
+//        D = 128 the accumulators fill TMEM and P_i overwrites the first 64
+//        columns of S_i, which its own thread has finished reading.
+//
+// Shared memory: two Q tiles, then a ring of K and V blocks; every tile is
+// stored as 128-row x 64-element (128-byte) chunks in the TMA 128-byte
+// swizzle, which is also the layout the MMA's matrix descriptors name.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "ptx.cuh"
+
+namespace fa {
+
+constexpr int kBM = 128;                 // query rows per tile
+constexpr int kBN = 128;                 // keys per block
+constexpr int kNumQ = 2;                 // query tiles per CTA
+constexpr int kRowsPerCta = kBM * kNumQ;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kTmemCols = 512;
+// A rescale of O is skipped while the running maximum grows by at most this
+// much (log2 units): probabilities then stay below 2^8, which fp16, bf16 and
+// the fp32 accumulators hold exactly as well as values below 1.
+constexpr float kRescaleThreshold = 8.0f;
+
+enum : unsigned { kStatusTimeout = 1u };
+
+struct FwdParams {
+  void *o;            // [BH, Nq, D] output
+  float *lse;         // [BH, Nq] output
+  int Nq, Nk;         // query and key rows per head
+  int n_units;        // work units per head: ceil(Nq / 256)
+  int causal;
+  float c;            // scale * log2(e), > 0
+  unsigned long long timeout_ns;
+  unsigned *status;   // device status word (timeout flags)
+};
+
+template <int D>
+struct Layout {
+  static constexpr int kChunks = D / 64;               // 128-byte chunks per row
+  static constexpr int kChunkBytes = kBM * 128;        // 16 KB
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kStages = D == 64 ? 4 : 2;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kNumQ * kTileBytes;
+  static constexpr int kV = kK + kStages * kTileBytes;
+  static constexpr int kBars = kV + kStages * kTileBytes;
+  // barrier indices
+  static constexpr int bQFull = 0;
+  static constexpr int bKFull = 1;
+  static constexpr int bVFull = bKFull + kStages;
+  static constexpr int bKVEmpty = bVFull + kStages;
+  static constexpr int bSFull = bKVEmpty + kStages;
+  static constexpr int bPFull = bSFull + kNumQ;
+  static constexpr int bOFinal = bPFull + kNumQ;
+  static constexpr int bDrain = bOFinal + kNumQ;
+  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int kMisc = kBars + kNumBars * 8;   // tmem base, abort flag
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;         // room to align to 1 KB
+  // TMEM columns
+  __host__ __device__ static constexpr uint32_t tS(int i) { return i * 128; }
+  __host__ __device__ static constexpr uint32_t tO(int i) { return 256 + i * D; }
+  __host__ __device__ static constexpr uint32_t tP(int i) { return D == 64 ? 384 + i * 64 : i * 128; }
+};
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, both
+// operands fp16 or both bf16, A K-major, B K-major or MN-major, M x N.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool bf16,
+                                                  bool b_mn_major) {
+  return (1u << 4)                                  // D format: f32
+         | ((bf16 ? 1u : 0u) << 7)                  // A format
+         | ((bf16 ? 1u : 0u) << 10)                 // B format
+         | ((b_mn_major ? 1u : 0u) << 16)           // B major-ness
+         | ((uint32_t)(N >> 3) << 17)               // N / 8
+         | ((uint32_t)(M >> 4) << 24);              // M / 16
+}
+
+// Shared-memory matrix descriptor for the 128-byte swizzle: start address,
+// leading- and stride-dimension byte offsets, the fixed version field, and
+// the swizzle mode.
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo,
+                                               uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// A bounded wait on an mbarrier phase.  Gives up when the CTA's abort flag is
+// set or after timeout_ns of global time; on a timeout it sets the abort flag
+// and records the timeout in the device status word.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
+                                           volatile int *abort_flag,
+                                           const FwdParams &p) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (*abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+        *abort_flag = 1;
+        atomicOr(p.status, (unsigned)kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// A wait used only while draining on the way out: bounded by the timeout
+// alone (it must not give up just because the CTA is aborting).
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity,
+                                           const FwdParams &p) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (;;) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+      atomicOr(p.status, (unsigned)kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+template <int D, bool kBF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
+                  const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV,
+                  const FwdParams p) {
+  using L = Layout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t *smem = smem_raw + (sbase - raw);
+  const uint32_t bars = sbase + L::kBars;
+  auto bar = [&](int idx) -> uint32_t { return bars + 8u * (uint32_t)idx; };
+  volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + L::kMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work unit: (head bh, 256-row unit), longest first when causal
+  const int bh = blockIdx.x / p.n_units;
+  int unit = blockIdx.x % p.n_units;
+  if (p.causal) unit = p.n_units - 1 - unit;
+  const int q0 = unit * kRowsPerCta;
+  int kv_end = p.Nk;
+  if (p.causal) kv_end = min(p.Nk, q0 + kRowsPerCta + (p.Nk - p.Nq));
+  const int nb = kv_end > 0 ? (kv_end + kBN - 1) / kBN : 0;
+
+  // ---- set-up: TMEM, barriers
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(sbase + L::kMisc, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(L::bQFull), 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      ptx::mbar_init(bar(L::bKFull + s), 1);
+      ptx::mbar_init(bar(L::bVFull + s), 1);
+      ptx::mbar_init(bar(L::bKVEmpty + s), 1);
+    }
+    for (int i = 0; i < kNumQ; ++i) {
+      ptx::mbar_init(bar(L::bSFull + i), 1);
+      ptx::mbar_init(bar(L::bPFull + i), kBM);
+      ptx::mbar_init(bar(L::bOFinal + i), 1);
+    }
+    ptx::mbar_init(bar(L::bDrain), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmK);
+    ptx::prefetch_tmap(&tmV);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kLoadWarp) {
+    // ================================================= TMA producer
+    if (lane == 0 && nb > 0) {
+      const uint64_t pol_q = ptx::policy_evict_first();
+      const uint64_t pol_kv = ptx::policy_evict_last();
+      ptx::mbar_arrive_expect_tx(bar(L::bQFull), kNumQ * L::kTileBytes);
+      for (int i = 0; i < kNumQ; ++i)
+        for (int c = 0; c < L::kChunks; ++c)
+          ptx::tma_load_3d(sbase + L::kQ + i * L::kTileBytes + c * L::kChunkBytes,
+                           &tmQ, bar(L::bQFull), c * 64, q0 + i * kBM, bh, pol_q);
+      int issued = 0;
+      for (int j = 0; j < nb; ++j) {
+        const int st = j % L::kStages;
+        const int use = j / L::kStages;
+        if (use > 0 &&
+            !wait_phase(bar(L::bKVEmpty + st), (use - 1) & 1, abort_flag, p))
+          break;
+        ptx::mbar_arrive_expect_tx(bar(L::bKFull + st), L::kTileBytes);
+        for (int c = 0; c < L::kChunks; ++c)
+          ptx::tma_load_3d(sbase + L::kK + st * L::kTileBytes + c * L::kChunkBytes,
+                           &tmK, bar(L::bKFull + st), c * 64, j * kBN, bh, pol_kv);
+        ptx::mbar_arrive_expect_tx(bar(L::bVFull + st), L::kTileBytes);
+        for (int c = 0; c < L::kChunks; ++c)
+          ptx::tma_load_3d(sbase + L::kV + st * L::kTileBytes + c * L::kChunkBytes,
+                           &tmV, bar(L::bVFull + st), c * 64, j * kBN, bh, pol_kv);
+        issued = j + 1;
+      }
+      // Drain: every copy this thread issued has landed before the CTA may
+      // exit (returns at once on the normal path).
+      wait_drain(bar(L::bQFull), 0, p);
+      for (int j = issued - L::kStages; j < issued; ++j) {
+        if (j < 0) continue;
+        const int st = j % L::kStages;
+        const uint32_t ph = (uint32_t)(j / L::kStages) & 1u;
+        wait_drain(bar(L::bKFull + st), ph, p);
+        wait_drain(bar(L::bVFull + st), ph, p);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ================================================= MMA issuer
+    if (lane == 0 && nb > 0) {
+      constexpr uint32_t idesc_s = make_idesc(kBM, kBN, kBF16, false);
+      constexpr uint32_t idesc_o = make_idesc(kBM, D, kBF16, true);
+      auto issue_s = [&](int i, int st) {
+        const uint32_t qa = sbase + L::kQ + i * L::kTileBytes;
+        const uint32_t ka = sbase + L::kK + st * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
+          ptx::mma_ss(tmem + L::tS(i), make_sdesc(qa + off, 16, 1024),
+                      make_sdesc(ka + off, 16, 1024), idesc_s, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int i, int st, bool acc) {
+        const uint32_t va = sbase + L::kV + st * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          ptx::mma_ts(tmem + L::tO(i), tmem + L::tP(i) + kk * 8,
+                      make_sdesc(va + kk * 16 * 128, L::kChunkBytes, 1024),
+                      idesc_o, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = wait_phase(bar(L::bQFull), 0, abort_flag, p) &&
+                wait_phase(bar(L::bKFull + 0), 0, abort_flag, p);
+      if (ok) {
+        ptx::tc_fence_after();
+        for (int i = 0; i < kNumQ; ++i) {
+          issue_s(i, 0);
+          ptx::mma_commit(bar(L::bSFull + i));
+        }
+      }
+      for (int j = 0; ok && j < nb; ++j) {
+        const int st = j % L::kStages;
+        if (!wait_phase(bar(L::bVFull + st), (j / L::kStages) & 1, abort_flag, p)) break;
+        const int st2 = (j + 1) % L::kStages;
+        for (int i = 0; i < kNumQ; ++i) {
+          if (!wait_phase(bar(L::bPFull + i), j & 1, abort_flag, p)) { ok = false; break; }
+          ptx::tc_fence_after();
+          issue_pv(i, st, j > 0);
+          if (j == nb - 1) ptx::mma_commit(bar(L::bOFinal + i));
+          if (i == kNumQ - 1) ptx::mma_commit(bar(L::bKVEmpty + st));
+          if (j + 1 < nb) {
+            if (i == 0) {
+              if (!wait_phase(bar(L::bKFull + st2), ((j + 1) / L::kStages) & 1,
+                              abort_flag, p)) { ok = false; break; }
+              ptx::tc_fence_after();
+            }
+            issue_s(i, st2);
+            ptx::mma_commit(bar(L::bSFull + i));
+          }
+        }
+      }
+      // Every MMA issued has completed before TMEM is released.
+      ptx::mma_commit(bar(L::bDrain));
+      wait_drain(bar(L::bDrain), 0, p);
+    }
+  } else {
+    // ================================================= softmax warpgroups
+    const int i = warp >> 2;                  // query tile of this warpgroup
+    const int r = threadIdx.x & 127;          // row within the tile = TMEM lane
+    const int row = q0 + i * kBM + r;         // query row within the head
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t tS = tmem + lane_off + L::tS(i);
+    const uint32_t tO = tmem + lane_off + L::tO(i);
+    const uint32_t tP = tmem + lane_off + L::tP(i);
+    const float c = p.c;
+    // keys [0, key_lim) are visible to this row
+    const int key_lim = p.causal ? min(p.Nk, row + 1 + (p.Nk - p.Nq)) : p.Nk;
+    float m = -CUDART_INF_F;   // running max of the scaled logits (log2 units)
+    float l = 0.f;             // running sum of exp2(logit - m)
+    bool ok = true;
+
+    for (int j = 0; j < nb; ++j) {
+      if (!wait_phase(bar(L::bSFull + i), j & 1, abort_flag, p)) { ok = false; break; }
+      ptx::tc_fence_after();
+      uint32_t s[kBN];
+#pragma unroll
+      for (int cc = 0; cc < kBN / 32; ++cc)
+        ptx::tmem_ld32(tS + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[cc * 32]));
+      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int cc = 0; cc < kBN / 32; ++cc)
+        ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&s[cc * 32]));
+      float *sf = reinterpret_cast<float *>(s);
+
+      const int lim = key_lim - j * kBN;   // columns >= lim are masked
+      if (lim < kBN) {
+#pragma unroll
+        for (int cc = 0; cc < kBN; ++cc)
+          if (cc >= lim) sf[cc] = -CUDART_INF_F;
+      }
+      float mx0 = sf[0], mx1 = sf[1], mx2 = sf[2], mx3 = sf[3];
+#pragma unroll
+      for (int cc = 4; cc < kBN; cc += 4) {
+        mx0 = fmaxf(mx0, sf[cc]);
+        mx1 = fmaxf(mx1, sf[cc + 1]);
+        mx2 = fmaxf(mx2, sf[cc + 2]);
+        mx3 = fmaxf(mx3, sf[cc + 3]);
+      }
+      const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      const float m_new = fmaxf(m, m_blk);
+      float m_use, alpha;
+      if (m_new == -CUDART_INF_F) {        // nothing visible yet
+        m_use = 0.f;
+        alpha = 1.f;
+      } else if (m_new - m > kRescaleThreshold) {
+        m_use = m_new;
+        alpha = ptx::ex2_approx(m - m_new);   // 0 when m is -inf
+      } else {
+        m_use = m;
+        alpha = 1.f;
+      }
+      const float neg_m = -m_use;
+      float rs0 = 0.f, rs1 = 0.f;
+      uint32_t pk[kBN / 2];
+#pragma unroll
+      for (int cc = 0; cc < kBN; cc += 2) {
+        const float p0 = ptx::ex2_approx(fmaf(sf[cc], c, neg_m));
+        const float p1 = ptx::ex2_approx(fmaf(sf[cc + 1], c, neg_m));
+        rs0 += p0;
+        rs1 += p1;
+        pk[cc / 2] = kBF16 ? ptx::pack_bf16(p0, p1) : ptx::pack_f16(p0, p1);
+      }
+#pragma unroll
+      for (int cc = 0; cc < kBN / 2; cc += 32)
+        ptx::tmem_st32(tP + cc, *reinterpret_cast<uint32_t(*)[32]>(&pk[cc]));
+      // O_i += P_i V_{j-1} has completed (tracked by the commit of S_i(j)):
+      // rescale the accumulator now if any row of this warp needs it.
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          ptx::tmem_ld32(tO + cc * 32, o);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence32(o);
+#pragma unroll
+          for (int t = 0; t < 32; ++t)
+            o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+          ptx::tmem_st32(tO + cc * 32, o);
+        }
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(L::bPFull + i));
+      l = l * alpha + (rs0 + rs1);
+      if (m_new != -CUDART_INF_F) m = m_use;
+    }
+
+    // ---- epilogue: O / l and LSE
+    if (ok && nb > 0) ok = wait_phase(bar(L::bOFinal + i), 0, abort_flag, p);
+    if (ok) {
+      ptx::tc_fence_after();
+      const bool valid = row < p.Nq;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const size_t orow = (size_t)bh * (size_t)p.Nq + (size_t)row;
+      uint16_t *optr = reinterpret_cast<uint16_t *>(p.o) + orow * D;
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        if (nb > 0) {
+          ptx::tmem_ld32(tO + cc * 32, o);
+          ptx::tmem_wait_ld();
+          ptx::reg_fence32(o);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) o[t] = 0u;
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const float a = __uint_as_float(o[2 * t]) * inv;
+          const float b = __uint_as_float(o[2 * t + 1]) * inv;
+          w[t] = kBF16 ? ptx::pack_bf16(a, b) : ptx::pack_f16(a, b);
+        }
+        if (valid) {
+          uint4 *dst = reinterpret_cast<uint4 *>(optr + cc * 32);
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+        }
+      }
+      if (valid)
+        p.lse[orow] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+    }
+  }
+
+  // ---- teardown: all TMEM traffic of the CTA is complete before release
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace fa

@@ -1,0 +1,113 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact attention forward library.
+ *
+ * The one operation: the exact, IO-aware attention forward pass
+ *
+ *     O   = softmax(scale * Q K^T [+ causal mask]) V
+ *     LSE = per-row natural-log logsumexp of the scaled, masked logits
+ *
+ * "Scale, mask, softmax and weighted sum" fused into one kernel is how the
+ * FlashAttention + TensorRT 10 page describes the fused attention
+ * computation (zzycbzc.com/news/393333, section "算子融合的极致优化",
+ * item 2).  The IO-aware part -- split the work into blocks that fit in
+ * on-chip memory so the N x N matrix never goes to HBM -- is the same
+ * page's section "FlashAttention的技术革命", and the "0 MB (recompute)"
+ * attention-matrix column of the Flash Attention 2 memory table on the
+ * benchmarks page (baguaai.com/zh/skills/benchmarks-332e54, "内存使用分析").
+ * The causal flag is the "causal": True setting, required for
+ * autoregressive models (2kiu.com/news/1440730, section 3.2).
+ *
+ * The library computes in fp32 from fp16 or bf16 inputs (mixed precision,
+ * 2kiu.com/news/1440730 section 1, item 1) on tcgen05 tensor cores.
+ * There is no CPU fallback: every call runs the CUDA kernel or fails.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream); NULL is the legacy default
+ * stream. */
+struct CUstream_st;
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_NULL = 1,           /* a required pointer is NULL                 */
+    FA_ERR_SHAPE = 2,          /* B, H or N negative, or too large           */
+    FA_ERR_HEADDIM = 3,        /* d is not 64 or 128                         */
+    FA_ERR_DTYPE = 4,          /* dtype is not FA_FP16 or FA_BF16            */
+    FA_ERR_ALIGN = 5,          /* q/k/v/o not 16-byte aligned, lse not 4-byte */
+    FA_ERR_SCALE = 6,          /* scale is not finite and positive           */
+    FA_ERR_CUDA = 7,           /* a CUDA runtime/driver call failed, or the
+                                  device is not sm_103 / lacks resources     */
+    FA_ERR_DEVICE_TIMEOUT = 8  /* a bounded on-device wait ran out; the
+                                  outputs of that launch are undefined      */
+} fa_status;
+
+typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype;
+
+/*
+ * fa_fwd -- attention forward for B*H independent (batch, head) problems.
+ *
+ *   q, k, v : device pointers, [B, H, N, d] contiguous, element type dtype.
+ *   o       : device pointer, [B, H, N, d] contiguous, element type dtype
+ *             (written).
+ *   lse     : device pointer, [B, H, N] contiguous fp32 (written):
+ *             lse[i] = ln(sum over allowed j of exp(scale * q_i . k_j)).
+ *   B, H, N : batch, heads, sequence length (queries and keys alike).
+ *             Any N >= 1 is accepted; B, H or N equal to 0 is an empty
+ *             problem and returns FA_OK without launching anything.
+ *   d       : head dimension, 64 or 128.
+ *   causal  : nonzero masks key j for query i when j > i.
+ *   scale   : multiplier of the logits (usually 1/sqrt(d)); finite and
+ *             > 0.
+ *   dtype   : FA_FP16 or FA_BF16 (inputs and output alike).
+ *   stream  : the CUDA stream the kernel is enqueued on.
+ *
+ * Ownership: all buffers belong to the caller and must stay valid until
+ * the work on `stream` completes.  The library allocates no device memory
+ * and keeps no pointer after the call returns.
+ *
+ * Errors: argument checks happen on the host before anything is enqueued;
+ * on any error nothing is launched and the outputs are untouched.  The call
+ * is asynchronous: it returns after the launch is enqueued.  Faults on the
+ * device (a bounded wait that ran out) are reported by
+ * fa_last_device_error().  Pointers to the same buffer for q, k and v are
+ * allowed; o and lse must not overlap the inputs or each other.
+ */
+FA_API fa_status fa_fwd(const void *q, const void *k, const void *v, void *o,
+                 float *lse, int B, int H, int N, int d, int causal,
+                 float scale, fa_dtype dtype, fa_stream_t stream);
+
+/* A static, human-readable description of a status code. */
+FA_API const char *fa_status_string(fa_status status);
+
+/*
+ * fa_last_device_error -- synchronise `stream`, then report and clear the
+ * device-side status word of the current device.
+ *
+ * Every wait inside the kernel is bounded in time; a wait that runs out
+ * records a flag in a per-device status word and the kernel returns
+ * early (its TMEM released).  This call returns FA_ERR_DEVICE_TIMEOUT if
+ * any launch since the previous call recorded such a flag, FA_ERR_CUDA if
+ * the synchronisation itself failed, and FA_OK otherwise.
+ */
+FA_API fa_status fa_last_device_error(fa_stream_t stream);
+
+/* The library's version as major * 10000 + minor * 100 + patch. */
+FA_API int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,216 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded, rounded inputs.
+
+Tolerances (O compared in fp64 against the unrounded oracle O; max and mean
+of |dO| over every compared element):
+    fp16 inputs: max <= 5e-3, mean <= 5e-4
+    bf16 inputs: max <= 2e-2, mean <= 2e-3
+    LSE (fp32):  max |dLSE| <= 1e-3
+Full-size workloads run on the GPU exactly as the benchmark launches them;
+the oracle then checks sampled (batch, head) slices, and sampled rows for
+the long-context case.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_39_gb300 as fa
+from exact_attention_39_gb300 import workloads as W
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"fp16": (5e-3, 5e-4), "bf16": (2e-2, 2e-3)}
+LSE_TOL = 1e-3
+
+
+def run_gpu(w, q, k, v):
+    dev = torch.device("cuda")
+    o, lse = fa.fwd(q.to(dev), k.to(dev), v.to(dev), causal=w.causal,
+                    scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
+    return o.cpu(), lse.cpu()
+
+
+def as64(t):
+    return t.double().numpy()
+
+
+def check(w, o_gpu, lse_gpu, q, k, v, heads=None, rows=None):
+    """Compare GPU outputs with the oracle on the (b, h) pairs ``heads``
+    (all when None) and query ``rows`` (all when None)."""
+    if heads is None:
+        qs, ks, vs = as64(q), as64(k), as64(v)
+        og, lg = as64(o_gpu), as64(lse_gpu)
+    else:
+        idx = torch.tensor([b * w.H + h for b, h in heads])
+        flat = lambda t: t.reshape(w.B * w.H, *t.shape[2:])[idx]
+        qs, ks, vs = as64(flat(q)), as64(flat(k)), as64(flat(v))
+        og, lg = as64(flat(o_gpu)), as64(flat(lse_gpu))
+    if rows is not None:
+        og, lg = og[..., rows, :], lg[..., rows]
+    o_ref, lse_ref = oracle.attention_fwd(qs, ks, vs, w.scale, w.causal, rows=rows)
+    assert np.isfinite(og).all() and np.isfinite(lg).all()
+    d_o = np.abs(og - o_ref)
+    d_l = np.abs(lg - lse_ref)
+    mx, mean = TOL[w.dtype]
+    msg = "%s: max|dO|=%.3g mean|dO|=%.3g max|dLSE|=%.3g" % (
+        w.name, d_o.max(), d_o.mean(), d_l.max())
+    assert d_o.max() <= mx and d_o.mean() <= mean and d_l.max() <= LSE_TOL, msg
+    return d_o.max(), d_o.mean(), d_l.max()
+
+
+def full_check(w):
+    q, k, v = W.make_inputs(w)
+    o, lse = run_gpu(w, q, k, v)
+    return check(w, o, lse, q, k, v)
+
+
+# ------------------------------------------------------------ the five configs
+def test_config_tiny():
+    full_check(W.TINY)
+
+
+@pytest.mark.parametrize("w", [W.N512, W.N512_Q8], ids=lambda w: w.name)
+def test_config_n512_fp16(w):
+    full_check(w)
+
+
+@pytest.mark.parametrize("w", [W.N2048_CAUSAL, W.N2048], ids=lambda w: w.name)
+def test_config_n2048_bf16(w):
+    q, k, v = W.make_inputs(w)
+    o, lse = run_gpu(w, q, k, v)
+    check(w, o, lse, q, k, v, heads=W.sample_heads(w, 16))
+
+
+@pytest.mark.parametrize("w", [W.N8192, W.N8192_CAUSAL], ids=lambda w: w.name)
+def test_config_n8192_bf16(w):
+    q, k, v = W.make_inputs(w)
+    o, lse = run_gpu(w, q, k, v)
+    check(w, o, lse, q, k, v, heads=W.sample_heads(w, 4))
+
+
+def test_config_long_context_d128():
+    w = W.LONG
+    q, k, v = W.make_inputs(w)
+    o, lse = run_gpu(w, q, k, v)
+    check(w, o, lse, q, k, v, heads=W.sample_heads(w, 2),
+          rows=W.sample_rows(w.N, 256))
+
+
+@pytest.mark.parametrize("n", [512, 1024, 4096])
+@pytest.mark.parametrize("causal", [False, True])
+def test_sequence_sweep(n, causal):
+    w = W.N8192.with_(name="sweep%d" % n, N=n, causal=causal)
+    q, k, v = W.make_inputs(w)
+    o, lse = run_gpu(w, q, k, v)
+    check(w, o, lse, q, k, v, heads=W.sample_heads(w, 2))
+
+
+# ------------------------------------------------------------ ragged and small
+@pytest.mark.parametrize("n", [1, 2, 3, 64, 127, 128, 129, 255, 256, 257, 300, 640, 1000])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_lengths_d64(n, causal):
+    for dtype in ("fp16", "bf16"):
+        w = W.Workload("ragged", 1, 3, n, 64, dtype, causal, seed=n)
+        full_check(w)
+
+
+@pytest.mark.parametrize("n", [1, 100, 128, 256, 383, 512, 777])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_lengths_d128(n, causal):
+    for dtype in ("fp16", "bf16"):
+        w = W.Workload("ragged128", 2, 2, n, 128, dtype, causal, seed=n + 1)
+        full_check(w)
+
+
+def test_large_logits_d128():
+    w = W.Workload("q8_d128", 1, 4, 700, 128, "fp16", False, seed=5, q_mult=8.0)
+    full_check(w)
+    full_check(w.with_(causal=True))
+
+
+# ------------------------------------------------------------ closed forms on the GPU
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_query_is_mean_of_values(d, causal):
+    n = 400
+    w = W.Workload("zeroq", 1, 2, n, d, "bf16", causal, seed=3)
+    q, k, v = W.make_inputs(w)
+    q = torch.zeros_like(q)
+    o, lse = run_gpu(w, q, k, v)
+    vd = v.double()
+    cnt = torch.arange(1, n + 1, dtype=torch.float64) if causal else torch.full((n,), float(n), dtype=torch.float64)
+    mean = vd.cumsum(2) / cnt[:, None] if causal else vd.mean(2, keepdim=True).expand_as(vd)
+    assert (o.double() - mean).abs().max() <= 2e-2
+    assert (lse.double() - cnt.log()).abs().max() <= 1e-3
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_constant_values(dtype):
+    w = W.Workload("constv", 2, 2, 333, 64, dtype, True, seed=4)
+    q, k, v = W.make_inputs(w)
+    row = torch.linspace(-3, 3, 64).to(W.DTYPES[dtype])
+    v = row.expand_as(v).contiguous()
+    o, _ = run_gpu(w, q, k, v)
+    # every softmax row sums to one, so O reproduces the constant row
+    # (up to the final rounding into the dtype and the 16-bit P)
+    assert (o.double() - row.double()).abs().max() <= (4e-3 if dtype == "fp16" else 3e-2)
+
+
+def test_single_key_and_causal_first_row():
+    w = W.Workload("first", 1, 2, 1, 64, "fp16", False, seed=6)
+    q, k, v = W.make_inputs(w)
+    o, lse = run_gpu(w, q, k, v)
+    assert torch.equal(o, v)          # one key: O = v0 exactly
+    dot = (q.double() * k.double()).sum(-1) * w.scale
+    assert (lse.double() - dot).abs().max() <= 1e-3
+    w = W.Workload("first", 1, 2, 500, 64, "fp16", True, seed=6)
+    q, k, v = W.make_inputs(w)
+    o, _ = run_gpu(w, q, k, v)
+    assert torch.equal(o[:, :, 0], v[:, :, 0])   # causal row 0 sees key 0 only
+
+
+# ------------------------------------------------------------ launch behaviour
+def test_deterministic_and_stream_ordered():
+    w = W.N2048_CAUSAL.with_(B=2)
+    q, k, v = (t.cuda() for t in W.make_inputs(w))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o1, l1 = fa.fwd(q, k, v, causal=True, stream=s)
+        o2, l2 = fa.fwd(q, k, v, causal=True, stream=s)
+    s.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert fa.last_device_error(s) == 0
+
+
+def test_host_buffers_end_to_end():
+    w = W.N512.with_(B=2, H=4)
+    q, k, v = W.make_inputs(w)
+    pin = lambda t: t.pin_memory()
+    qh, kh, vh = pin(q), pin(k), pin(v)
+    dev = [torch.empty_like(t, device="cuda") for t in (q, k, v)]
+    od = torch.empty_like(dev[0])
+    ld = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device="cuda")
+    oh = torch.empty_like(q).pin_memory()
+    lh = torch.empty(w.B, w.H, w.N, dtype=torch.float32).pin_memory()
+    fa.fwd_host(qh, kh, vh, *dev, od, ld, oh, lh, causal=False, scale=w.scale)
+    check(w, oh, lh, q, k, v)
+
+
+def test_outputs_do_not_touch_neighbours():
+    # O and LSE are written only inside their [B, H, N, d] / [B, H, N] spans.
+    w = W.Workload("guard", 1, 2, 300, 64, "bf16", True, seed=8)
+    q, k, v = (t.cuda() for t in W.make_inputs(w))
+    n_o = q.numel()
+    buf = torch.full((n_o + 2048,), 7.0, dtype=q.dtype, device="cuda")
+    lbuf = torch.full((w.B * w.H * w.N + 256,), 7.0, dtype=torch.float32, device="cuda")
+    o = buf[1024:1024 + n_o].view_as(q)
+    lse = lbuf[128:128 + w.B * w.H * w.N].view(w.B, w.H, w.N)
+    fa.fwd(q, k, v, causal=True, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert (buf[:1024] == 7).all() and (buf[1024 + n_o:] == 7).all()
+    assert (lbuf[:128] == 7).all() and (lbuf[128 + w.B * w.H * w.N:] == 7).all()
