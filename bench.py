@@ -1,0 +1,369 @@
+"""Benchmark of the attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+
+One step is one fa_fwd launch over the whole workload (default: batch 8,
+32 heads, N = 8192, head dim 64, bf16, non-causal -- the headline shape of
+the pages' forward-time tables).  Inputs are seeded synthetic N(0, 1) data
+already resident in HBM; they are 805 MB, larger than the 129 MB L2, so
+no flush is needed between steps.  The metric is the attention-forward
+throughput, 4*B*H*N^2*d counted FLOPs per step (half when causal), in
+TFLOPS.  Prints one JSON line on rank 0.
+
+Under torchrun (N > 1) every rank runs its own copy of the workload on its
+own GPU (independent (batch, head) problems: no data exchange); value is
+the FLOPs of all ranks over the slowest rank's time.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead,
+on a bounded sample of the same workload per step (rank 0 only).
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from exact_attention_39_gb300 import workloads as W  # noqa: E402
+
+METRIC = "attn fwd TFLOPS & % of GB300 BF16 tensor peak (B8 H32 d64, N=512–8192)"
+UNIT = "TFLOPS"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+WORKLOADS = {w.name: w for w in
+             [W.TINY, W.N512, W.N512_Q8, W.N2048, W.N2048_CAUSAL, W.N8192,
+              W.N8192_CAUSAL, W.LONG] + W.sweep(False) + W.sweep(True)}
+DEFAULT_WORKLOAD = W.N8192.name
+CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw",
+                "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown",
+                "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown",
+                "clocks_event_reasons.sw_power_cap"]
+
+
+# ---------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_ms, local_units, world):
+    """Max of the per-rank times and sum of the per-rank work units over
+    the process group (identity for one process).  Returns (ms, units)."""
+    if world == 1:
+        return float(local_ms), float(local_units)
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) \
+        if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=dev)
+    u = torch.tensor([float(local_units)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    def __init__(self, gpu_index, period_ms=50):
+        self.gpu_index = gpu_index
+        self.period_ms = period_ms
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        out_dir = os.path.join(ROOT, "gpurun_out")
+        os.makedirs(out_dir, exist_ok=True)
+        self.path = os.path.join(out_dir, "clocks_%d.csv" % os.getpid())
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index),
+                 "--query-gpu=" + ",".join(CLOCK_FIELDS), "--format=csv,noheader,nounits",
+                 "-lms", str(self.period_ms)], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == len(CLOCK_FIELDS):
+                    rows.append(dict(zip(CLOCK_FIELDS, parts)))
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        power = [num(r["power.draw"]) for r in rows]
+        sm = [num(r["clocks.sm"]) for r in rows]
+        pmax = max(p for p in power if p is not None) if any(p is not None for p in power) else None
+        # "under load": samples drawing at least half of the peak power seen
+        loaded = [s for s, p in zip(sm, power)
+                  if s is not None and (pmax is None or (p is not None and p >= 0.5 * pmax))]
+        reasons = set()
+        for r in rows:
+            for key in CLOCK_FIELDS[5:]:
+                if r[key].lower() == "active":
+                    reasons.add(key.split(".")[-1])
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": num(rows[0]["clocks.max.sm"]),
+                "power_w_max": pmax,
+                "samples": len(rows),
+                "reasons": sorted(reasons)}
+
+
+def time_oracle(w, budget_s, max_heads):
+    """Time the fp64 oracle on whole heads of ``w`` until ``budget_s`` of
+    work is done.  Returns (seconds, flops, heads, threads)."""
+    import oracle
+    q, k, v = W.make_inputs(w.with_(B=1, H=max_heads))
+    nt = oracle.default_threads()
+    flops, secs, heads = 0.0, 0.0, 0
+    for h in range(max_heads):
+        qh, kh, vh = (t[0, h].double().numpy() for t in (q, k, v))
+        t0 = time.perf_counter()
+        oracle.attention_fwd(qh, kh, vh, w.scale, w.causal, nthreads=nt)
+        secs += time.perf_counter() - t0
+        flops += w.with_(B=1, H=1).flops()
+        heads += 1
+        if secs >= budget_s:
+            break
+    return secs, flops, heads, nt
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args, w, world, rank):
+    """The oracle on the host cores: each step is a bounded sample of the
+    workload (a block of query rows of one head)."""
+    if rank != 0:
+        return None
+    import numpy as np
+    import oracle
+    rows = min(w.N, args.ref_rows)
+    q, k, v = W.make_inputs(w.with_(B=1, H=1))
+    qh, kh, vh = (t[0, 0].double().numpy() for t in (q, k, v))
+    sel = np.arange(rows, dtype=np.int64) * (w.N // rows)
+    nt = oracle.default_threads()
+    row_flops = 4.0 * w.n_keys * w.d / (2.0 if w.causal else 1.0)
+    for _ in range(args.warmup):
+        oracle.attention_fwd(qh, kh, vh, w.scale, w.causal, rows=sel, nthreads=nt)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention_fwd(qh, kh, vh, w.scale, w.causal, rows=sel, nthreads=nt)
+    secs = time.perf_counter() - t0
+    value = row_flops * rows * args.steps / secs / 1e12
+    sample = ("%d query rows (every %d-th) of one head of %s per step, fp64, "
+              "%d threads" % (rows, w.N // rows, w.name, nt))
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": nt,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def run_gpu(args, w, world, rank, local):
+    import exact_attention_39_gb300 as fa
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wr = w.with_(seed=w.seed + rank)
+    q_h, k_h, v_h = W.make_inputs(wr)
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        fa.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse,
+               stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    if fa.last_device_error(stream) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        stream.synchronize()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    region_ms = starts[0].elapsed_time(ends[-1])
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if fa.last_device_error(stream) != 0:
+        raise RuntimeError("device status set during the timed region")
+
+    ms, flops_all = aggregate(region_ms, w.flops() * args.steps, world)
+    value = flops_all / (ms * 1e-3) / 1e12
+    ms_per_step = ms / args.steps
+    kern_avg_ms = sum(kernel_ms) / len(kernel_ms)
+
+    # ---- end to end through the public API: host buffers, copies timed
+    e2e = None
+    if not args.no_e2e:
+        pin = [t.pin_memory() for t in (q_h, k_h, v_h)]
+        o_h = torch.empty_like(q_h).pin_memory()
+        l_h = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        for _ in range(2):
+            fa.fwd_host(*pin, q, k, v, o, lse, o_h, l_h, causal=w.causal,
+                        scale=w.scale, stream=stream)
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            fa.fwd_host(*pin, q, k, v, o, lse, o_h, l_h, causal=w.causal,
+                        scale=w.scale, stream=stream)
+        e_ms = (time.perf_counter() - t0) * 1e3
+        barrier(world)
+        e_ms, e_flops = aggregate(e_ms, w.flops() * e2e_steps, world)
+        h2d = sum(t.numel() * t.element_size() for t in pin)
+        d2h = o_h.numel() * o_h.element_size() + l_h.numel() * l_h.element_size()
+        e2e = {"value": e_flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": e2e_steps, "ms_per_step": e_ms / e2e_steps}
+
+    if rank != 0:
+        return None
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = w.flops() / (kern_avg_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % src
+                if src == "measured" else "fallback 1.9 PFLOP/s bf16",
+                "traffic": args.traffic,
+                "algorithmic_bytes": w.hbm_bytes(),
+                "kernel_ms": kern_avg_ms,
+                "hbm_gbs_algorithmic": w.hbm_bytes() / (kern_avg_ms * 1e-3) / 1e9}
+    cpu = None
+    if not args.no_cpu_baseline:
+        secs, fl, heads, nt = time_oracle(w, args.cpu_budget, args.cpu_max_heads)
+        cpu = {"value": fl / secs / 1e12, "unit": UNIT, "cores": nt,
+               "kind": "oracle",
+               "sample": "%d whole head(s) (all %d query rows) of %s, fp64, %.1f s"
+                         % (heads, w.N, w.name, secs)}
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "global_batch": w.B * world,
+                   "seq_len": w.N, "parallelism": "independent heads per GPU" if world > 1 else "1 GPU",
+                   "l2": "inputs %d MB > 129 MB L2, no flush" % (3 * w.B * w.H * w.N * w.d * 2 // 10 ** 6)},
+        "gpu_launches": args.steps,
+        "pct_of_peak": 100.0 * achieved / peak,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clocks.summary(),
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--cpu-max-heads", type=int, default=16)
+    ap.add_argument("--ref-rows", type=int, default=1024,
+                    help="query rows per reference step")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch from an ncu capture of this kernel")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "gb300" and args.steps > 3:
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    world, rank, local = dist_env()
+    w = WORKLOADS[args.workload]
+    if world > 1 and args.impl == "gb300":
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        if args.impl == "reference":
+            line = run_reference(args, w, world, rank)
+        else:
+            line = run_gpu(args, w, world, rank, local)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1 and args.impl == "gb300":
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -15,6 +15,8 @@
 //              thread t of a warpgroup owns query row t = TMEM lane t
 //   warp  8    TMA producer: Q tiles once, then K/V blocks into a ring
 //   warp  9    TMEM allocator and tcgen05 MMA issuer (one thread)
+//   warps 10-11 idle (they complete the third warpgroup, which lets the
+//              register budget be moved to the softmax warpgroups)
 //
 // Per key block j the MMA thread issues, in this order,
 //   PV_0(j-1)... i.e.   O_0 += P_0 V_j ; S_0 = Q_0 K_{j+1}^T ;
@@ -50,7 +52,12 @@ constexpr int kNumQ = 2;                 // query tiles per CTA
 constexpr int kRowsPerCta = kBM * kNumQ;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;            // three warpgroups; warps 10-11 idle
+// Register split: launched at 168 per thread (65536 / 384, rounded down to
+// a multiple of 8); the producer/MMA warpgroup gives registers back to the
+// two softmax warpgroups.  128*88 + 256*208 = 64512 <= 384*168 = 64512.
+constexpr uint32_t kRegsControl = 88;
+constexpr uint32_t kRegsSoftmax = 208;
 constexpr int kTmemCols = 512;
 // A rescale of O is skipped while the running maximum grows by at most this
 // much (log2 units): probabilities then stay below 2^8, which fp16, bf16 and
@@ -85,14 +92,18 @@ struct Layout {
   static constexpr int bKFull = 1;
   static constexpr int bVFull = bKFull + kStages;
   static constexpr int bKVEmpty = bVFull + kStages;
-  static constexpr int bSFull = bKVEmpty + kStages;
-  static constexpr int bPFull = bSFull + kNumQ;
-  static constexpr int bOFinal = bPFull + kNumQ;
-  static constexpr int bDrain = bOFinal + kNumQ;
+  static constexpr int bSFull = bKVEmpty + kStages;   // S_i ready (MMA commit)
+  static constexpr int bSFree = bSFull + kNumQ;       // S_i read into registers
+  static constexpr int bPFull = bSFree + kNumQ;       // P_i written, O_i rescaled
+  static constexpr int bODone = bPFull + kNumQ;       // O_i += P_i V_j done (commit)
+  static constexpr int bDrain = bODone + kNumQ;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kMisc = kBars + kNumBars * 8;   // tmem base, abort flag
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;         // room to align to 1 KB
+  // With D = 64, P has TMEM columns of its own, so the MMA for the next
+  // block's scores may overwrite S_i as soon as softmax has read it.
+  static constexpr bool kEarlyS = D == 64;
   // TMEM columns
   __host__ __device__ static constexpr uint32_t tS(int i) { return i * 128; }
   __host__ __device__ static constexpr uint32_t tO(int i) { return 256 + i * D; }
@@ -143,6 +154,14 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
       }
     }
   }
+}
+
+// wait_phase executed by all 32 lanes of a warp, with one warp-wide verdict.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
+                                          volatile int *abort_flag,
+                                          const FwdParams &p) {
+  const bool ok = wait_phase(bar, parity, abort_flag, p);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // A wait used only while draining on the way out: bounded by the timeout
@@ -201,8 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kNumQ; ++i) {
       ptx::mbar_init(bar(L::bSFull + i), 1);
+      ptx::mbar_init(bar(L::bSFree + i), kBM);
       ptx::mbar_init(bar(L::bPFull + i), kBM);
-      ptx::mbar_init(bar(L::bOFinal + i), 1);
+      ptx::mbar_init(bar(L::bODone + i), 1);
     }
     ptx::mbar_init(bar(L::bDrain), 1);
     *abort_flag = 0;
@@ -218,35 +238,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kLoadWarp) {
+  if (warp >= 8) {
+   ptx::regs_dec<kRegsControl>();
+   // The producer and MMA warps run their loops with all 32 lanes, so every
+   // operand is warp-uniform; one elected lane issues each copy, MMA and
+   // commit (a commit tracks the MMAs of the lane that issues it).
+   if (warp == kLoadWarp) {
     // ================================================= TMA producer
-    if (lane == 0 && nb > 0) {
+    if (nb > 0) {
+      const bool leader = ptx::elect_one();
       const uint64_t pol_q = ptx::policy_evict_first();
       const uint64_t pol_kv = ptx::policy_evict_last();
-      ptx::mbar_arrive_expect_tx(bar(L::bQFull), kNumQ * L::kTileBytes);
-      for (int i = 0; i < kNumQ; ++i)
-        for (int c = 0; c < L::kChunks; ++c)
-          ptx::tma_load_3d(sbase + L::kQ + i * L::kTileBytes + c * L::kChunkBytes,
-                           &tmQ, bar(L::bQFull), c * 64, q0 + i * kBM, bh, pol_q);
+      if (leader) {
+        ptx::mbar_arrive_expect_tx(bar(L::bQFull), kNumQ * L::kTileBytes);
+        for (int i = 0; i < kNumQ; ++i)
+          for (int c = 0; c < L::kChunks; ++c)
+            ptx::tma_load_3d(sbase + L::kQ + i * L::kTileBytes + c * L::kChunkBytes,
+                             &tmQ, bar(L::bQFull), c * 64, q0 + i * kBM, bh, pol_q);
+      }
       int issued = 0;
       for (int j = 0; j < nb; ++j) {
         const int st = j % L::kStages;
         const int use = j / L::kStages;
         if (use > 0 &&
-            !wait_phase(bar(L::bKVEmpty + st), (use - 1) & 1, abort_flag, p))
+            !wait_warp(bar(L::bKVEmpty + st), (use - 1) & 1, abort_flag, p))
           break;
-        ptx::mbar_arrive_expect_tx(bar(L::bKFull + st), L::kTileBytes);
-        for (int c = 0; c < L::kChunks; ++c)
-          ptx::tma_load_3d(sbase + L::kK + st * L::kTileBytes + c * L::kChunkBytes,
-                           &tmK, bar(L::bKFull + st), c * 64, j * kBN, bh, pol_kv);
-        ptx::mbar_arrive_expect_tx(bar(L::bVFull + st), L::kTileBytes);
-        for (int c = 0; c < L::kChunks; ++c)
-          ptx::tma_load_3d(sbase + L::kV + st * L::kTileBytes + c * L::kChunkBytes,
-                           &tmV, bar(L::bVFull + st), c * 64, j * kBN, bh, pol_kv);
+        if (leader) {
+          ptx::mbar_arrive_expect_tx(bar(L::bKFull + st), L::kTileBytes);
+          for (int c = 0; c < L::kChunks; ++c)
+            ptx::tma_load_3d(sbase + L::kK + st * L::kTileBytes + c * L::kChunkBytes,
+                             &tmK, bar(L::bKFull + st), c * 64, j * kBN, bh, pol_kv);
+          ptx::mbar_arrive_expect_tx(bar(L::bVFull + st), L::kTileBytes);
+          for (int c = 0; c < L::kChunks; ++c)
+            ptx::tma_load_3d(sbase + L::kV + st * L::kTileBytes + c * L::kChunkBytes,
+                             &tmV, bar(L::bVFull + st), c * 64, j * kBN, bh, pol_kv);
+        }
         issued = j + 1;
       }
-      // Drain: every copy this thread issued has landed before the CTA may
-      // exit (returns at once on the normal path).
+      // Drain: every copy issued has landed before the CTA may exit
+      // (returns at once on the normal path).
       wait_drain(bar(L::bQFull), 0, p);
       for (int j = issued - L::kStages; j < issued; ++j) {
         if (j < 0) continue;
@@ -258,64 +288,88 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ================================================= MMA issuer
-    if (lane == 0 && nb > 0) {
+    if (nb > 0) {
+      const bool leader = ptx::elect_one();
       constexpr uint32_t idesc_s = make_idesc(kBM, kBN, kBF16, false);
       constexpr uint32_t idesc_o = make_idesc(kBM, D, kBF16, true);
+      // Descriptors are built once; stepping through a tile only adds to the
+      // 14-bit start-address field (address >> 4, all smem offsets < 256 KB).
+      const uint64_t dq0 = make_sdesc(sbase + L::kQ, 16, 1024);
+      const uint64_t dk0 = make_sdesc(sbase + L::kK, 16, 1024);
+      const uint64_t dv0 = make_sdesc(sbase + L::kV, L::kChunkBytes, 1024);
+      // S_i = Q_i K_st^T, then a commit on s_full[i]
       auto issue_s = [&](int i, int st) {
-        const uint32_t qa = sbase + L::kQ + i * L::kTileBytes;
-        const uint32_t ka = sbase + L::kK + st * L::kTileBytes;
+        const uint64_t dq = dq0 + (uint64_t)((i * L::kTileBytes) >> 4);
+        const uint64_t dk = dk0 + (uint64_t)((st * L::kTileBytes) >> 4);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
-          ptx::mma_ss(tmem + L::tS(i), make_sdesc(qa + off, 16, 1024),
-                      make_sdesc(ka + off, 16, 1024), idesc_s, kk > 0);
-        }
-      };
-      auto issue_pv = [&](int i, int st, bool acc) {
-        const uint32_t va = sbase + L::kV + st * L::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          ptx::mma_ts(tmem + L::tO(i), tmem + L::tP(i) + kk * 8,
-                      make_sdesc(va + kk * 16 * 128, L::kChunkBytes, 1024),
-                      idesc_o, (acc || kk > 0) ? 1u : 0u);
-        }
-      };
-      bool ok = wait_phase(bar(L::bQFull), 0, abort_flag, p) &&
-                wait_phase(bar(L::bKFull + 0), 0, abort_flag, p);
-      if (ok) {
-        ptx::tc_fence_after();
-        for (int i = 0; i < kNumQ; ++i) {
-          issue_s(i, 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
+            ptx::mma_ss(tmem + L::tS(i), dq + off, dk + off, idesc_s, kk > 0);
+          }
           ptx::mma_commit(bar(L::bSFull + i));
         }
+      };
+      // O_i (+)= P_i V_st, then a commit on o_done[i]
+      auto issue_pv = [&](int i, int st, bool acc) {
+        const uint64_t dv = dv0 + (uint64_t)((st * L::kTileBytes) >> 4);
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            ptx::mma_ts(tmem + L::tO(i), tmem + L::tP(i) + kk * 8,
+                        dv + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
+                        (acc || kk > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(bar(L::bODone + i));
+        }
+      };
+      bool ok = wait_warp(bar(L::bQFull), 0, abort_flag, p) &&
+                wait_warp(bar(L::bKFull + 0), 0, abort_flag, p);
+      if (ok) {
+        ptx::tc_fence_after();
+        for (int i = 0; i < kNumQ; ++i) issue_s(i, 0);
       }
       for (int j = 0; ok && j < nb; ++j) {
         const int st = j % L::kStages;
-        if (!wait_phase(bar(L::bVFull + st), (j / L::kStages) & 1, abort_flag, p)) break;
         const int st2 = (j + 1) % L::kStages;
+        const bool more = j + 1 < nb;
+        if (L::kEarlyS && more) {
+          // Scores of block j+1 as soon as each softmax warpgroup has its
+          // block-j scores in registers.
+          if (!wait_warp(bar(L::bKFull + st2), ((j + 1) / L::kStages) & 1, abort_flag, p)) break;
+          for (int i = 0; i < kNumQ && ok; ++i) {
+            if (!wait_warp(bar(L::bSFree + i), j & 1, abort_flag, p)) { ok = false; break; }
+            ptx::tc_fence_after();
+            issue_s(i, st2);
+          }
+          if (!ok) break;
+        }
+        if (!wait_warp(bar(L::bVFull + st), (j / L::kStages) & 1, abort_flag, p)) break;
         for (int i = 0; i < kNumQ; ++i) {
-          if (!wait_phase(bar(L::bPFull + i), j & 1, abort_flag, p)) { ok = false; break; }
+          if (!wait_warp(bar(L::bPFull + i), j & 1, abort_flag, p)) { ok = false; break; }
           ptx::tc_fence_after();
           issue_pv(i, st, j > 0);
-          if (j == nb - 1) ptx::mma_commit(bar(L::bOFinal + i));
-          if (i == kNumQ - 1) ptx::mma_commit(bar(L::bKVEmpty + st));
-          if (j + 1 < nb) {
+          if (i == kNumQ - 1 && leader) ptx::mma_commit(bar(L::bKVEmpty + st));
+          if (!L::kEarlyS && more) {
+            // P_i shares columns with S_i: the next scores go in only after
+            // O_i += P_i V_j (the tensor pipe runs one thread's MMAs in order).
             if (i == 0) {
-              if (!wait_phase(bar(L::bKFull + st2), ((j + 1) / L::kStages) & 1,
-                              abort_flag, p)) { ok = false; break; }
+              if (!wait_warp(bar(L::bKFull + st2), ((j + 1) / L::kStages) & 1,
+                             abort_flag, p)) { ok = false; break; }
               ptx::tc_fence_after();
             }
             issue_s(i, st2);
-            ptx::mma_commit(bar(L::bSFull + i));
           }
         }
       }
       // Every MMA issued has completed before TMEM is released.
-      ptx::mma_commit(bar(L::bDrain));
+      if (leader) ptx::mma_commit(bar(L::bDrain));
       wait_drain(bar(L::bDrain), 0, p);
     }
+   }
   } else {
     // ================================================= softmax warpgroups
+    ptx::regs_inc<kRegsSoftmax>();
     const int i = warp >> 2;                  // query tile of this warpgroup
     const int r = threadIdx.x & 127;          // row within the tile = TMEM lane
     const int row = q0 + i * kBM + r;         // query row within the head
@@ -330,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l = 0.f;             // running sum of exp2(logit - m)
     bool ok = true;
 
+    const float2 c2 = make_float2(c, c);
     for (int j = 0; j < nb; ++j) {
       if (!wait_phase(bar(L::bSFull + i), j & 1, abort_flag, p)) { ok = false; break; }
       ptx::tc_fence_after();
@@ -341,6 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < kBN / 32; ++cc)
         ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&s[cc * 32]));
+      if (L::kEarlyS) {
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::bSFree + i));
+      }
       float *sf = reinterpret_cast<float *>(s);
 
       const int lim = key_lim - j * kBN;   // columns >= lim are masked
@@ -349,15 +408,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < kBN; ++cc)
           if (cc >= lim) sf[cc] = -CUDART_INF_F;
       }
-      float mx0 = sf[0], mx1 = sf[1], mx2 = sf[2], mx3 = sf[3];
+      // row maximum: eight independent chains of three-input max
+      float mx[8];
 #pragma unroll
-      for (int cc = 4; cc < kBN; cc += 4) {
-        mx0 = fmaxf(mx0, sf[cc]);
-        mx1 = fmaxf(mx1, sf[cc + 1]);
-        mx2 = fmaxf(mx2, sf[cc + 2]);
-        mx3 = fmaxf(mx3, sf[cc + 3]);
+      for (int t = 0; t < 8; ++t) mx[t] = sf[t];
+#pragma unroll
+      for (int cc = 8; cc < kBN; cc += 16) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          mx[t] = ptx::fmax3(mx[t], sf[cc + t], cc + 8 + t < kBN ? sf[cc + 8 + t] : sf[t]);
       }
-      const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      const float m_blk = ptx::fmax3(ptx::fmax3(mx[0], mx[1], mx[2]),
+                                     ptx::fmax3(mx[3], mx[4], mx[5]),
+                                     fmaxf(mx[6], mx[7])) * c;
       const float m_new = fmaxf(m, m_blk);
       float m_use, alpha;
       if (m_new == -CUDART_INF_F) {        // nothing visible yet
@@ -370,23 +433,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_use = m;
         alpha = 1.f;
       }
-      const float neg_m = -m_use;
-      float rs0 = 0.f, rs1 = 0.f;
+      // p = 2^(s*c - m): scale and shift two at a time, four partial sums
+      const float2 nm2 = make_float2(-m_use, -m_use);
+      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       uint32_t pk[kBN / 2];
 #pragma unroll
       for (int cc = 0; cc < kBN; cc += 2) {
-        const float p0 = ptx::ex2_approx(fmaf(sf[cc], c, neg_m));
-        const float p1 = ptx::ex2_approx(fmaf(sf[cc + 1], c, neg_m));
-        rs0 += p0;
-        rs1 += p1;
+        const float2 x = __ffma2_rn(make_float2(sf[cc], sf[cc + 1]), c2, nm2);
+        const float p0 = ptx::ex2_approx(x.x);
+        const float p1 = ptx::ex2_approx(x.y);
+        rs[(cc >> 1) & 3] = __fadd2_rn(rs[(cc >> 1) & 3], make_float2(p0, p1));
         pk[cc / 2] = kBF16 ? ptx::pack_bf16(p0, p1) : ptx::pack_f16(p0, p1);
+      }
+      // O_i += P_i V_{j-1} must be complete before P_i is overwritten and
+      // before O_i is rescaled.
+      if (j > 0) {
+        if (!wait_phase(bar(L::bODone + i), (j - 1) & 1, abort_flag, p)) { ok = false; break; }
+        ptx::tc_fence_after();
       }
 #pragma unroll
       for (int cc = 0; cc < kBN / 2; cc += 32)
         ptx::tmem_st32(tP + cc, *reinterpret_cast<uint32_t(*)[32]>(&pk[cc]));
-      // O_i += P_i V_{j-1} has completed (tracked by the commit of S_i(j)):
-      // rescale the accumulator now if any row of this warp needs it.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
@@ -394,20 +464,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_wait_ld();
           ptx::reg_fence32(o);
 #pragma unroll
-          for (int t = 0; t < 32; ++t)
-            o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+          for (int t = 0; t < 32; t += 2) {
+            const float2 v2 = __fmul2_rn(make_float2(__uint_as_float(o[t]),
+                                                     __uint_as_float(o[t + 1])), a2);
+            o[t] = __float_as_uint(v2.x);
+            o[t + 1] = __float_as_uint(v2.y);
+          }
           ptx::tmem_st32(tO + cc * 32, o);
         }
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(L::bPFull + i));
-      l = l * alpha + (rs0 + rs1);
+      const float2 r01 = __fadd2_rn(rs[0], rs[1]);
+      const float2 r23 = __fadd2_rn(rs[2], rs[3]);
+      l = l * alpha + ((r01.x + r01.y) + (r23.x + r23.y));
       if (m_new != -CUDART_INF_F) m = m_use;
     }
 
     // ---- epilogue: O / l and LSE
-    if (ok && nb > 0) ok = wait_phase(bar(L::bOFinal + i), 0, abort_flag, p);
+    if (ok && nb > 0) ok = wait_phase(bar(L::bODone + i), (nb - 1) & 1, abort_flag, p);
     if (ok) {
       ptx::tc_fence_after();
       const bool valid = row < p.Nq;
