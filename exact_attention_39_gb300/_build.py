@@ -9,6 +9,7 @@ LIB_NAME = "libfa_sm103.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 SOURCES = ["fa_api.cu"]
 DEPS = ["fa_fwd_kernel.cuh", "ptx.cuh"]
+HEADERS = ["fa.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -23,7 +24,7 @@ def _stale():
         return True
     t = os.path.getmtime(LIB_PATH)
     inputs = [os.path.join(CSRC, f) for f in SOURCES + DEPS]
-    inputs.append(os.path.join(INCLUDE, "fa.h"))
+    inputs += [os.path.join(INCLUDE, h) for h in HEADERS]
     return any(os.path.getmtime(f) > t for f in inputs)
 
 

@@ -1,0 +1,66 @@
+"""The benchmark's multi-process host logic on CPU: two gloo ranks, max of
+the per-rank times and sum of the per-rank work (no GPU, no data path)."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port),
+                      RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        assert bench.dist_env() == (world, rank, rank)
+        bench.barrier(world)
+        ms, units = bench.aggregate(10.0 + rank * 5.0, 100.0 * (rank + 1), world)
+        q.put((rank, ms, units))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_aggregation():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(world))
+    for rank, ms, units in got:
+        assert ms == 15.0          # slowest rank's time
+        assert units == 300.0      # work of all ranks
+
+
+def test_single_process_identity():
+    assert bench.aggregate(3.5, 7.0, 1) == (3.5, 7.0)
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    class A:
+        steps, warmup, ref_rows = 1, 0, 8
+    w = bench.WORKLOADS["b8h32n512d64_bf16"]
+    assert bench.run_reference(A, w, 2, 1) is None
+    line = bench.run_reference(A, w, 2, 0)
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_kernel_hash_is_stable():
+    assert bench.kernel_source_hash() == bench.kernel_source_hash()
+    assert len(bench.kernel_source_hash()) == 16
