@@ -17,6 +17,11 @@ the FLOPs of all ranks over the slowest rank's time.
 
 ``--impl reference`` times the fp64 CPU oracle on the host cores instead,
 on a bounded sample of the same workload per step (rank 0 only).
+
+``--impl standard`` times the unfused "standard" attention the pages compare
+against (score matrix materialised in HBM, softmax, second product; torch
+and cuBLAS on the GPU, one batch element at a time to bound memory).  It is
+a comparator for the pages' "标准" columns, not a check of results.
 """
 import argparse
 import json
@@ -237,6 +242,50 @@ def run_reference(args, w, world, rank):
     }
 
 
+def run_standard(args, w, world, rank, local):
+    """Unfused attention on the GPU with library calls: S = scale * Q K^T in
+    the input dtype, softmax in fp32, O = P V.  Same FLOP count as fa_fwd."""
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q, k, v = (t.to(dev) for t in W.make_inputs(w.with_(seed=w.seed + rank)))
+    o = torch.empty_like(q)
+    mask = None
+    if w.causal:
+        mask = torch.ones(w.N, w.n_keys, dtype=torch.bool, device=dev).tril(w.n_keys - w.N)
+
+    def step():
+        for b in range(w.B):
+            s_ = torch.matmul(q[b], k[b].transpose(-1, -2)) * w.scale
+            if mask is not None:
+                s_ = s_.masked_fill(~mask, float("-inf"))
+            p_ = torch.softmax(s_.float(), dim=-1).to(q.dtype)
+            torch.matmul(p_, v[b], out=o[b])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize(dev)
+    ms, flops_all = aggregate(t0.elapsed_time(t1), w.flops() * args.steps, world)
+    if rank != 0:
+        return None
+    value = flops_all / (ms * 1e-3) / 1e12
+    return {"impl": "standard", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N,
+                       "d": w.d, "causal": w.causal,
+                       "method": "materialised S (dtype), fp32 softmax, torch/cuBLAS"}}
+
+
 def run_gpu(args, w, world, rank, local):
     import exact_attention_39_gb300 as fa
 
@@ -349,7 +398,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--impl", choices=["gb300", "reference", "standard"], default="gb300")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -366,19 +415,21 @@ def main(argv=None):
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
     world, rank, local = dist_env()
     w = WORKLOADS[args.workload]
-    if world > 1 and args.impl == "gb300":
+    if world > 1 and args.impl in ("gb300", "standard"):
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     try:
         if args.impl == "reference":
             line = run_reference(args, w, world, rank)
+        elif args.impl == "standard":
+            line = run_standard(args, w, world, rank, local)
         else:
             line = run_gpu(args, w, world, rank, local)
         if line is not None:
             print(json.dumps(line), flush=True)
     finally:
-        if world > 1 and args.impl == "gb300":
+        if world > 1 and args.impl in ("gb300", "standard"):
             import torch.distributed as dist
             dist.destroy_process_group()
 

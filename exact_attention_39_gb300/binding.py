@@ -25,7 +25,8 @@ FA_ERR_DEVICE_TIMEOUT = 8
 FA_FP16 = 0
 FA_BF16 = 1
 
-EXPORTED = ("fa_fwd", "fa_status_string", "fa_last_device_error", "fa_version")
+EXPORTED = ("fa_fwd", "fa_fwd_qk", "fa_status_string", "fa_last_device_error",
+            "fa_version")
 
 _lib = None
 
@@ -50,6 +51,8 @@ def load_library(path=None):
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     lib.fa_fwd.restype = i
+    lib.fa_fwd_qk.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_qk.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_device_error.argtypes = [vp]
@@ -84,6 +87,15 @@ def fa_fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, causal,
                                  float(scale), int(dtype_code), stream_handle)
 
 
+def fa_fwd_qk_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d,
+                  causal, scale, dtype_code, stream_handle):
+    """The C call for different query and key lengths; returns the status."""
+    return load_library().fa_fwd_qk(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr,
+                                    int(B), int(H), int(Nq), int(Nk), int(d),
+                                    int(bool(causal)), float(scale),
+                                    int(dtype_code), stream_handle)
+
+
 def _dtype_code(t):
     if t.dtype == torch.float16:
         return FA_FP16
@@ -93,35 +105,46 @@ def _dtype_code(t):
 
 
 def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None):
-    """Attention forward on CUDA tensors ``q, k, v`` of shape [B, H, N, d].
+    """Attention forward on CUDA tensors q [B, H, Nq, d], k and v [B, H, Nk, d].
 
-    Returns ``(o, lse)``: ``o`` like ``q``; ``lse`` [B, H, N] float32.
-    ``scale`` defaults to 1/sqrt(d).  The kernel is enqueued on ``stream``
-    (default: the current torch stream); nothing is synchronised.
+    Returns ``(o, lse)``: ``o`` like ``q``; ``lse`` [B, H, Nq] float32.
+    With Nq != Nk the causal mask is aligned to the bottom-right corner
+    (key j visible to query i iff j <= i + Nk - Nq).  ``scale`` defaults to
+    1/sqrt(d).  The kernel is enqueued on ``stream`` (default: the current
+    torch stream); nothing is synchronised.
     """
-    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
-        raise ValueError("q, k, v must all be [B, H, N, d] with equal shapes")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q must be [B, H, Nq, d] and k, v [B, H, Nk, d]")
+    if k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]:
+        raise ValueError("q, k, v must agree in B, H and d")
     if not (q.dtype == k.dtype == v.dtype):
         raise TypeError("q, k, v must share one dtype")
     code = _dtype_code(q)
     for t in (q, k, v):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("q, k, v must be contiguous CUDA tensors")
-    B, H, N, d = q.shape
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
-        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
         raise ValueError("out must be a contiguous tensor like q")
-    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    if lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, Nq] tensor")
     with torch.cuda.device(q.device):
-        _check(fa_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                          out.data_ptr(), lse.data_ptr(), B, H, N, d, causal,
-                          scale, code, _stream_handle(stream)))
+        if Nq == Nk:
+            st = fa_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                            out.data_ptr(), lse.data_ptr(), B, H, Nq, d,
+                            causal, scale, code, _stream_handle(stream))
+        else:
+            st = fa_fwd_qk_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                               out.data_ptr(), lse.data_ptr(), B, H, Nq, Nk, d,
+                               causal, scale, code, _stream_handle(stream))
+        _check(st)
     return out, lse
 
 

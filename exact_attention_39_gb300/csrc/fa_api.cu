@@ -109,21 +109,21 @@ bool aligned(const void *p, uintptr_t a) {
 
 extern "C" {
 
-fa_status fa_fwd(const void *q, const void *k, const void *v, void *o,
-                 float *lse, int B, int H, int N, int d, int causal,
-                 float scale, fa_dtype dtype, fa_stream_t stream) {
+fa_status fa_fwd_qk(const void *q, const void *k, const void *v, void *o,
+                    float *lse, int B, int H, int Nq, int Nk, int d, int causal,
+                    float scale, fa_dtype dtype, fa_stream_t stream) {
   using namespace fa;
-  if (B < 0 || H < 0 || N < 0) return FA_ERR_SHAPE;
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_HEADDIM;
   if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_DTYPE;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
-  if (B == 0 || H == 0 || N == 0) return FA_OK;   // empty problem
+  if (B == 0 || H == 0 || Nq == 0) return FA_OK;   // empty problem
   const long long bh = (long long)B * (long long)H;
-  const long long units = ((long long)N + kRowsPerCta - 1) / kRowsPerCta;
+  const long long units = ((long long)Nq + kRowsPerCta - 1) / kRowsPerCta;
   if (bh > (1ll << 31) - 1 || bh * units > (1ll << 31) - 1) return FA_ERR_SHAPE;
-  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
-      !aligned(lse, 4))
+  if (!q || !o || !lse || (Nk > 0 && (!k || !v))) return FA_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      (Nk > 0 && (!aligned(k, 16) || !aligned(v, 16))))
     return FA_ERR_ALIGN;
 
   int dev = 0;
@@ -132,16 +132,20 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o,
   if (st != FA_OK) return st;
 
   const bool bf16 = dtype == FA_BF16;
+  // With no keys the kernel loads nothing from K or V; their maps are
+  // built over q only to be well formed.
+  const void *kb = Nk > 0 ? k : q, *vb = Nk > 0 ? v : q;
+  const int nk_map = Nk > 0 ? Nk : Nq;
   CUtensorMap mq, mk, mv;
-  if (!encode_map(&mq, q, bf16, d, N, bh) || !encode_map(&mk, k, bf16, d, N, bh) ||
-      !encode_map(&mv, v, bf16, d, N, bh))
+  if (!encode_map(&mq, q, bf16, d, Nq, bh) || !encode_map(&mk, kb, bf16, d, nk_map, bh) ||
+      !encode_map(&mv, vb, bf16, d, nk_map, bh))
     return FA_ERR_CUDA;
 
   FwdParams p;
   p.o = o;
   p.lse = lse;
-  p.Nq = N;
-  p.Nk = N;
+  p.Nq = Nq;
+  p.Nk = Nk;
   p.n_units = (int)units;
   p.causal = causal ? 1 : 0;
   p.c = (float)((double)scale * 1.4426950408889634);
@@ -158,6 +162,13 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o,
     err = bf16 ? launch<128, true>(mq, mk, mv, p, grid, s)
                : launch<128, false>(mq, mk, mv, p, grid, s);
   return err == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd(const void *q, const void *k, const void *v, void *o,
+                 float *lse, int B, int H, int N, int d, int causal,
+                 float scale, fa_dtype dtype, fa_stream_t stream) {
+  if (N < 0) return FA_ERR_SHAPE;
+  return fa_fwd_qk(q, k, v, o, lse, B, H, N, N, d, causal, scale, dtype, stream);
 }
 
 const char *fa_status_string(fa_status status) {

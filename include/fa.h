@@ -88,6 +88,25 @@ FA_API fa_status fa_fwd(const void *q, const void *k, const void *v, void *o,
                  float *lse, int B, int H, int N, int d, int causal,
                  float scale, fa_dtype dtype, fa_stream_t stream);
 
+/*
+ * fa_fwd_qk -- the same forward pass with different query and key lengths.
+ *
+ *   q, o    : [B, H, Nq, d];  k, v : [B, H, Nk, d];  lse : [B, H, Nq] fp32.
+ *   causal  : key j is visible to query i iff j <= i + (Nk - Nq), i.e. the
+ *             mask is aligned to the bottom-right corner (the last query
+ *             sees every key; with Nq == Nk this is j <= i).  A query row
+ *             that sees no key (i < Nq - Nk) gets O = 0 and LSE = -inf, as
+ *             does every row when Nk == 0.
+ *   B, H or Nq equal to 0 is an empty problem (FA_OK, nothing launched);
+ *   Nk == 0 with Nq > 0 writes the all-masked result.  k and v may be NULL
+ *   when Nk == 0.  Everything else as fa_fwd, which equals
+ *   fa_fwd_qk(..., Nq = N, Nk = N, ...).
+ */
+FA_API fa_status fa_fwd_qk(const void *q, const void *k, const void *v,
+                           void *o, float *lse, int B, int H, int Nq, int Nk,
+                           int d, int causal, float scale, fa_dtype dtype,
+                           fa_stream_t stream);
+
 /* A static, human-readable description of a status code. */
 FA_API const char *fa_status_string(fa_status status);
 

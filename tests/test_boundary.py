@@ -69,11 +69,30 @@ def test_host_side_argument_checks(kw, code):
     assert call(**kw) == code
 
 
+def call_qk(q=P, k=P, v=P, o=P, lse=P, B=1, H=1, Nq=128, Nk=64, d=64, causal=1,
+            scale=0.125, dtype=b.FA_BF16):
+    return b.fa_fwd_qk_raw(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale,
+                           dtype, ctypes.c_void_p(0))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Nq=-1), b.FA_ERR_SHAPE), (dict(Nk=-1), b.FA_ERR_SHAPE),
+    (dict(k=NULL), b.FA_ERR_NULL), (dict(v=NULL), b.FA_ERR_NULL),
+    (dict(q=NULL), b.FA_ERR_NULL), (dict(k=P + 4), b.FA_ERR_ALIGN),
+    (dict(d=80), b.FA_ERR_HEADDIM), (dict(dtype=5), b.FA_ERR_DTYPE),
+    (dict(scale=-1.0), b.FA_ERR_SCALE),
+])
+def test_host_side_checks_qk(kw, code):
+    assert call_qk(**kw) == code
+
+
 def test_empty_problems_launch_nothing():
     # B, H or N equal to zero is an empty problem: FA_OK, nothing enqueued,
     # pointers never looked at.
     for kw in (dict(B=0), dict(H=0), dict(N=0)):
         assert call(q=NULL, k=NULL, v=NULL, o=NULL, lse=NULL, **kw) == b.FA_OK
+    for kw in (dict(B=0), dict(H=0), dict(Nq=0)):
+        assert call_qk(q=NULL, k=NULL, v=NULL, o=NULL, lse=NULL, **kw) == b.FA_OK
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="needs a machine without a GPU")
@@ -91,6 +110,8 @@ def test_python_wrapper_validation():
         fa.fwd(q, q, q[:, :, :64])
     with pytest.raises(TypeError):
         fa.fwd(q, q, q.half())
+    with pytest.raises(ValueError):
+        fa.fwd(q, q[:, :, :, :32], q[:, :, :, :32])
 
 
 def test_missing_library_fails_loudly(tmp_path):

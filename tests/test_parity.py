@@ -127,6 +127,34 @@ def test_ragged_lengths_d128(n, causal):
         full_check(w)
 
 
+@pytest.mark.parametrize("nq,nk", [(1, 1000), (64, 777), (300, 128), (128, 300),
+                                   (1000, 257), (257, 1000), (513, 2048), (2048, 100)])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_query_and_key_lengths_differ(nq, nk, causal, d):
+    # bottom-right causal alignment; rows that see no key give O = 0, LSE = -inf
+    w = W.Workload("qk", 1, 2, nq, d, "bf16" if d == 64 else "fp16", causal,
+                   seed=nq + nk, Nk=nk)
+    q, k, v = W.make_inputs(w)
+    o, lse = run_gpu(w, q, k, v)
+    n_dead = max(0, nq - nk) if causal else 0
+    if n_dead:
+        assert (o[:, :, :n_dead] == 0).all()
+        assert torch.isinf(lse[:, :, :n_dead]).all() and (lse[:, :, :n_dead] < 0).all()
+    live = list(range(n_dead, nq))
+    check(w, o, lse, q, k, v, rows=live)
+
+
+def test_no_keys_at_all():
+    w = W.Workload("nokeys", 2, 2, 200, 64, "bf16", False, seed=9, Nk=0)
+    q = W.make_inputs(w.with_(Nk=None))[0].cuda()
+    kv = torch.empty(2, 2, 0, 64, dtype=q.dtype, device="cuda")
+    o, lse = fa.fwd(q, kv, kv)
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
+    assert (o == 0).all() and torch.isinf(lse).all() and (lse < 0).all()
+
+
 def test_large_logits_d128():
     w = W.Workload("q8_d128", 1, 4, 700, 128, "fp16", False, seed=5, q_mult=8.0)
     full_check(w)
