@@ -46,7 +46,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
                   "bf16_tflops_sustained": 1700.0}
 WORKLOADS = {w.name: w for w in
              [W.TINY, W.N512, W.N512_Q8, W.N2048, W.N2048_CAUSAL, W.N8192,
-              W.N8192_CAUSAL, W.LONG] + W.sweep(False) + W.sweep(True)}
+              W.N8192_CAUSAL, W.LONG, W.N8192_E4M3, W.N8192_E4M3_CAUSAL]
+             + W.sweep(False) + W.sweep(True)}
 DEFAULT_WORKLOAD = W.N8192.name
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture of the kernel, keyed by a hash of the kernel sources and the
@@ -294,13 +295,19 @@ def run_gpu(args, w, world, rank, local):
     wr = w.with_(seed=w.seed + rank)
     q_h, k_h, v_h = W.make_inputs(wr)
     q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
-    o = torch.empty_like(q)
+    fp8 = w.dtype == "e4m3"
+    o = torch.empty(q.shape, dtype=torch.bfloat16 if fp8 else q.dtype, device=dev)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
     def step():
-        fa.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse,
-               stream=stream)
+        if fp8:
+            ds = W.E4M3_DESCALE
+            fa.fwd_fp8(q, k, v, ds, ds, ds, causal=w.causal, scale=w.scale,
+                       out=o, lse=lse, stream=stream)
+        else:
+            fa.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse,
+                   stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -332,7 +339,7 @@ def run_gpu(args, w, world, rank, local):
 
     # ---- end to end through the public API: host buffers, copies timed
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not fp8:
         pin = [t.pin_memory() for t in (q_h, k_h, v_h)]
         o_h = torch.empty_like(q_h).pin_memory()
         l_h = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
@@ -358,11 +365,16 @@ def run_gpu(args, w, world, rank, local):
         return None
     peaks, src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    # fp8 contractions: the measured bf16 peak times the nominal fp8/bf16
+    # dense ratio (4.5 / 2.25)
+    peak_mult = 2.0 if fp8 else 1.0
+    peak *= peak_mult
     achieved = w.flops() / (kern_avg_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % src
-                if src == "measured" else "fallback 1.9 PFLOP/s bf16",
+                "peak_source": ("%s bf16 burst (MEASURED_PEAKS.json)" % src
+                                if src == "measured" else "fallback 1.9 PFLOP/s bf16")
+                + (" x 2 (nominal fp8/bf16 ratio)" if fp8 else ""),
                 "traffic": args.traffic if args.traffic is not None else
                 MEASURED_TRAFFIC.get((kernel_source_hash(), w.name)),
                 "algorithmic_bytes": w.hbm_bytes(),

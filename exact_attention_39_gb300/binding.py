@@ -25,8 +25,8 @@ FA_ERR_DEVICE_TIMEOUT = 8
 FA_FP16 = 0
 FA_BF16 = 1
 
-EXPORTED = ("fa_fwd", "fa_fwd_qk", "fa_status_string", "fa_last_device_error",
-            "fa_version")
+EXPORTED = ("fa_fwd", "fa_fwd_qk", "fa_fwd_fp8", "fa_status_string",
+            "fa_last_device_error", "fa_version")
 
 _lib = None
 
@@ -53,6 +53,8 @@ def load_library(path=None):
     lib.fa_fwd.restype = i
     lib.fa_fwd_qk.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
     lib.fa_fwd_qk.restype = i
+    lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, f, f, vp]
+    lib.fa_fwd_fp8.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_device_error.argtypes = [vp]
@@ -94,6 +96,17 @@ def fa_fwd_qk_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d,
                                     int(B), int(H), int(Nq), int(Nk), int(d),
                                     int(bool(causal)), float(scale),
                                     int(dtype_code), stream_handle)
+
+
+def fa_fwd_fp8_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d,
+                   causal, scale, q_descale, k_descale, v_descale,
+                   stream_handle):
+    """The C call of the e4m3 forward; returns the status."""
+    return load_library().fa_fwd_fp8(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr,
+                                     int(B), int(H), int(Nq), int(Nk), int(d),
+                                     int(bool(causal)), float(scale),
+                                     float(q_descale), float(k_descale),
+                                     float(v_descale), stream_handle)
 
 
 def _dtype_code(t):
@@ -145,6 +158,39 @@ def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None):
                                out.data_ptr(), lse.data_ptr(), B, H, Nq, Nk, d,
                                causal, scale, code, _stream_handle(stream))
         _check(st)
+    return out, lse
+
+
+def fwd_fp8(q, k, v, q_descale, k_descale, v_descale, causal=False,
+            scale=None, out=None, lse=None, stream=None):
+    """Attention forward on float8_e4m3fn CUDA tensors (real values are
+    q * q_descale etc.); returns ``(o, lse)`` with ``o`` bf16 [B, H, Nq, d]."""
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q must be [B, H, Nq, d] and k, v [B, H, Nk, d]")
+    if k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]:
+        raise ValueError("q, k, v must agree in B, H and d")
+    for t in (q, k, v):
+        if t.dtype != torch.float8_e4m3fn:
+            raise TypeError("q, k, v must be torch.float8_e4m3fn")
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if out.shape != (B, H, Nq, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 [B, H, Nq, d] tensor")
+    if lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, Nq] tensor")
+    with torch.cuda.device(q.device):
+        _check(fa_fwd_fp8_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                              out.data_ptr(), lse.data_ptr(), B, H, Nq, Nk, d,
+                              causal, scale, q_descale, k_descale, v_descale,
+                              _stream_handle(stream)))
     return out, lse
 
 

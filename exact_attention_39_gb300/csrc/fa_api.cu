@@ -28,9 +28,9 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 bool g_dev_ready[kMaxDevices] = {};
 unsigned *g_status_ptr[kMaxDevices] = {};
 
-template <int D, bool BF16>
+template <int D, int T>
 void *kernel_ptr() {
-  return reinterpret_cast<void *>(&fa_fwd_kernel<D, BF16>);
+  return reinterpret_cast<void *>(&fa_fwd_kernel<D, T>);
 }
 
 // One-time, per-process and per-device set-up: the driver's tensor-map
@@ -53,11 +53,13 @@ fa_status ensure_ready(int dev) {
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return FA_ERR_CUDA;
   if (major != 10 || minor != 3) return FA_ERR_CUDA;   // built for sm_103a only
-  const void *kernels[4] = {kernel_ptr<64, false>(), kernel_ptr<64, true>(),
-                            kernel_ptr<128, false>(), kernel_ptr<128, true>()};
-  const int smem[4] = {Layout<64>::kAlloc, Layout<64>::kAlloc,
-                       Layout<128>::kAlloc, Layout<128>::kAlloc};
-  for (int t = 0; t < 4; ++t)
+  const void *kernels[6] = {kernel_ptr<64, kF16>(), kernel_ptr<64, kBF16>(),
+                            kernel_ptr<64, kE4M3>(), kernel_ptr<128, kF16>(),
+                            kernel_ptr<128, kBF16>(), kernel_ptr<128, kE4M3>()};
+  const int smem[6] = {Layout<64, kF16>::kAlloc, Layout<64, kBF16>::kAlloc,
+                       Layout<64, kE4M3>::kAlloc, Layout<128, kF16>::kAlloc,
+                       Layout<128, kBF16>::kAlloc, Layout<128, kE4M3>::kAlloc};
+  for (int t = 0; t < 6; ++t)
     if (cudaFuncSetAttribute(kernels[t], cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem[t]) != cudaSuccess)
       return FA_ERR_CUDA;
@@ -69,35 +71,80 @@ fa_status ensure_ready(int dev) {
   return FA_OK;
 }
 
-// [BH, rows, d] tensor viewed by TMA as a 3-D box grid of 64 x 128 x 1
-// elements (128-byte rows, 128-byte swizzle).  Rows past `rows` within a
-// head read as zero.
-bool encode_map(CUtensorMap *map, const void *base, bool bf16, int d, int rows,
-                long long bh) {
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)bh};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2u, (cuuint64_t)d * 2u * (cuuint64_t)rows};
-  cuuint32_t box[3] = {64u, 128u, 1u};
+// [BH, rows, d] tensor viewed by TMA as a 3-D box grid of (chunk width) x
+// 128 x 1 elements in the swizzle the kernel's layout names.  Rows past
+// `rows` within a head read as zero.
+template <int D, int T>
+bool encode_map(CUtensorMap *map, const void *base, int rows, long long bh) {
+  using L = Layout<D, T>;
+  const cuuint64_t eb = (cuuint64_t)Elem<T>::kBytes;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)bh};
+  cuuint64_t strides[2] = {(cuuint64_t)D * eb, (cuuint64_t)D * eb * (cuuint64_t)rows};
+  cuuint32_t box[3] = {(cuuint32_t)L::kChunkElems, (cuuint32_t)kBM, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = g_encode(map,
-                        bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                        3, const_cast<void *>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  const CUtensorMapDataType dt = T == kF16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                 : T == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUresult r = g_encode(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        L::kSwz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                       : CU_TENSOR_MAP_SWIZZLE_64B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <int D, bool BF16>
-cudaError_t launch(const CUtensorMap &mq, const CUtensorMap &mk,
-                   const CUtensorMap &mv, const FwdParams &p, unsigned grid,
-                   cudaStream_t stream) {
+// Encodes the maps and launches one forward kernel.  With no keys the
+// kernel loads nothing from K or V; their maps are built over q only to be
+// well formed.
+template <int D, int T>
+fa_status run(const void *q, const void *k, const void *v, FwdParams p,
+              long long bh, cudaStream_t stream) {
+  const void *kb = p.Nk > 0 ? k : q, *vb = p.Nk > 0 ? v : q;
+  const int nk_map = p.Nk > 0 ? p.Nk : p.Nq;
+  CUtensorMap mq, mk, mv;
+  if (!encode_map<D, T>(&mq, q, p.Nq, bh) || !encode_map<D, T>(&mk, kb, nk_map, bh) ||
+      !encode_map<D, T>(&mv, vb, nk_map, bh))
+    return FA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.gridDim = dim3((unsigned)(bh * p.n_units), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Layout<D>::kAlloc;
+  cfg.dynamicSmemBytes = Layout<D, T>::kAlloc;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, BF16>, mq, mk, mv, p);
+  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, T>, mq, mk, mv, p) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+bool aligned(const void *p, uintptr_t a);
+
+// Shared argument checks and set-up of fa_fwd_qk and fa_fwd_fp8.  Returns
+// FA_OK with *launch false for an empty problem.
+fa_status prepare(const void *q, const void *k, const void *v, const void *o,
+                  const float *lse, int B, int H, int Nq, int Nk, int d,
+                  float scale, long long *bh_out, long long *units_out,
+                  int *dev_out, bool *launch) {
+  *launch = false;
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+  if (B == 0 || H == 0 || Nq == 0) return FA_OK;   // empty problem
+  const long long bh = (long long)B * (long long)H;
+  const long long units = ((long long)Nq + kRowsPerCta - 1) / kRowsPerCta;
+  if (bh > (1ll << 31) - 1 || bh * units > (1ll << 31) - 1) return FA_ERR_SHAPE;
+  if (!q || !o || !lse || (Nk > 0 && (!k || !v))) return FA_ERR_NULL;
+  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      (Nk > 0 && (!aligned(k, 16) || !aligned(v, 16))))
+    return FA_ERR_ALIGN;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  fa_status st = ensure_ready(dev);
+  if (st != FA_OK) return st;
+  *bh_out = bh;
+  *units_out = units;
+  *dev_out = dev;
+  *launch = true;
+  return FA_OK;
 }
 
 bool aligned(const void *p, uintptr_t a) {
@@ -116,31 +163,12 @@ fa_status fa_fwd_qk(const void *q, const void *k, const void *v, void *o,
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0) return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_HEADDIM;
   if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_DTYPE;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
-  if (B == 0 || H == 0 || Nq == 0) return FA_OK;   // empty problem
-  const long long bh = (long long)B * (long long)H;
-  const long long units = ((long long)Nq + kRowsPerCta - 1) / kRowsPerCta;
-  if (bh > (1ll << 31) - 1 || bh * units > (1ll << 31) - 1) return FA_ERR_SHAPE;
-  if (!q || !o || !lse || (Nk > 0 && (!k || !v))) return FA_ERR_NULL;
-  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
-      (Nk > 0 && (!aligned(k, 16) || !aligned(v, 16))))
-    return FA_ERR_ALIGN;
-
+  long long bh = 0, units = 0;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  fa_status st = ensure_ready(dev);
-  if (st != FA_OK) return st;
-
-  const bool bf16 = dtype == FA_BF16;
-  // With no keys the kernel loads nothing from K or V; their maps are
-  // built over q only to be well formed.
-  const void *kb = Nk > 0 ? k : q, *vb = Nk > 0 ? v : q;
-  const int nk_map = Nk > 0 ? Nk : Nq;
-  CUtensorMap mq, mk, mv;
-  if (!encode_map(&mq, q, bf16, d, Nq, bh) || !encode_map(&mk, kb, bf16, d, nk_map, bh) ||
-      !encode_map(&mv, vb, bf16, d, nk_map, bh))
-    return FA_ERR_CUDA;
-
+  bool launch = false;
+  fa_status st = prepare(q, k, v, o, lse, B, H, Nq, Nk, d, scale, &bh, &units,
+                         &dev, &launch);
+  if (st != FA_OK || !launch) return st;
   FwdParams p;
   p.o = o;
   p.lse = lse;
@@ -149,19 +177,47 @@ fa_status fa_fwd_qk(const void *q, const void *k, const void *v, void *o,
   p.n_units = (int)units;
   p.causal = causal ? 1 : 0;
   p.c = (float)((double)scale * 1.4426950408889634);
+  p.o_scale = 1.f;
   p.timeout_ns = kTimeoutNs;
   p.status = g_status_ptr[dev];
-
-  const unsigned grid = (unsigned)(bh * units);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t err;
+  const bool bf16 = dtype == FA_BF16;
   if (d == 64)
-    err = bf16 ? launch<64, true>(mq, mk, mv, p, grid, s)
-               : launch<64, false>(mq, mk, mv, p, grid, s);
-  else
-    err = bf16 ? launch<128, true>(mq, mk, mv, p, grid, s)
-               : launch<128, false>(mq, mk, mv, p, grid, s);
-  return err == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    return bf16 ? run<64, kBF16>(q, k, v, p, bh, s) : run<64, kF16>(q, k, v, p, bh, s);
+  return bf16 ? run<128, kBF16>(q, k, v, p, bh, s) : run<128, kF16>(q, k, v, p, bh, s);
+}
+
+fa_status fa_fwd_fp8(const void *q, const void *k, const void *v, void *o,
+                     float *lse, int B, int H, int Nq, int Nk, int d, int causal,
+                     float scale, float q_descale, float k_descale,
+                     float v_descale, fa_stream_t stream) {
+  using namespace fa;
+  if (!std::isfinite(q_descale) || !std::isfinite(k_descale) ||
+      !std::isfinite(v_descale) || !(q_descale > 0.f) || !(k_descale > 0.f) ||
+      !(v_descale > 0.f))
+    return FA_ERR_SCALE;
+  long long bh = 0, units = 0;
+  int dev = 0;
+  bool launch = false;
+  fa_status st = prepare(q, k, v, o, lse, B, H, Nq, Nk, d, scale, &bh, &units,
+                         &dev, &launch);
+  if (st != FA_OK || !launch) return st;
+  const double c = (double)scale * (double)q_descale * (double)k_descale *
+                   1.4426950408889634;
+  if (!(c > 0.0) || !std::isfinite(c) || c > 3.0e38) return FA_ERR_SCALE;
+  FwdParams p;
+  p.o = o;
+  p.lse = lse;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.n_units = (int)units;
+  p.causal = causal ? 1 : 0;
+  p.c = (float)c;
+  p.o_scale = v_descale;
+  p.timeout_ns = kTimeoutNs;
+  p.status = g_status_ptr[dev];
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return d == 64 ? run<64, kE4M3>(q, k, v, p, bh, s) : run<128, kE4M3>(q, k, v, p, bh, s);
 }
 
 fa_status fa_fwd(const void *q, const void *k, const void *v, void *o,

@@ -72,17 +72,49 @@ struct FwdParams {
   int Nq, Nk;         // query and key rows per head
   int n_units;        // work units per head: ceil(Nq / 256)
   int causal;
-  float c;            // scale * log2(e), > 0
+  float c;            // scale * log2(e) (* q and k descales for e4m3), > 0
+  float o_scale;      // multiplies O before the division by l (v descale)
   unsigned long long timeout_ns;
   unsigned *status;   // device status word (timeout flags)
 };
 
-template <int D>
+// Element types of Q, K, V and of P in the second product.
+enum ElemType : int { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
+
+template <int T> struct Elem;
+template <> struct Elem<kF16> {
+  static constexpr int kBytes = 2;
+  static constexpr int kMmaK = 16;          // K of one tcgen05.mma (32 bytes)
+  static constexpr uint32_t kFmt = 0;       // instruction-descriptor format
+  static constexpr bool kF8 = false;
+};
+template <> struct Elem<kBF16> {
+  static constexpr int kBytes = 2;
+  static constexpr int kMmaK = 16;
+  static constexpr uint32_t kFmt = 1;
+  static constexpr bool kF8 = false;
+};
+template <> struct Elem<kE4M3> {
+  static constexpr int kBytes = 1;
+  static constexpr int kMmaK = 32;
+  static constexpr uint32_t kFmt = 0;
+  static constexpr bool kF8 = true;
+};
+
+template <int D, int T>
 struct Layout {
-  static constexpr int kChunks = D / 64;               // 128-byte chunks per row
-  static constexpr int kChunkBytes = kBM * 128;        // 16 KB
+  using E = Elem<T>;
+  // Tiles are stored as chunks of kBM rows x kSwz bytes in the TMA swizzle of
+  // the same width (128 bytes; 64 when a whole row is only 64 bytes).
+  static constexpr int kRowBytes = D * E::kBytes;
+  static constexpr int kSwz = kRowBytes < 128 ? kRowBytes : 128;
+  static constexpr int kChunkElems = kSwz / E::kBytes;
+  static constexpr int kChunks = D / kChunkElems;
+  static constexpr int kChunkBytes = kBM * kSwz;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = D == 64 ? 4 : 2;
+  static constexpr int kSBO = 8 * kSwz;                 // 8-row swizzle atom
+  static constexpr uint64_t kSwzMode = kSwz == 128 ? 2 : 4;   // descriptor code
+  static constexpr int kStages = kTileBytes <= 16384 ? 4 : 2;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kNumQ * kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
@@ -101,37 +133,43 @@ struct Layout {
   static constexpr int kMisc = kBars + kNumBars * 8;   // tmem base, abort flag
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;         // room to align to 1 KB
-  // With D = 64, P has TMEM columns of its own, so the MMA for the next
-  // block's scores may overwrite S_i as soon as softmax has read it.
-  static constexpr bool kEarlyS = D == 64;
+  // TMEM columns of one tile's P (four 8-bit or two 16-bit values a cell).
+  static constexpr int kPCols = kBN * E::kBytes / 4;
+  // When P fits beside the accumulators it has TMEM columns of its own, so
+  // the MMA for the next block's scores may overwrite S_i as soon as softmax
+  // has read it.
+  static constexpr bool kEarlyS = 256 + 2 * D + 2 * kPCols <= kTmemCols;
   // TMEM columns
   __host__ __device__ static constexpr uint32_t tS(int i) { return i * 128; }
   __host__ __device__ static constexpr uint32_t tO(int i) { return 256 + i * D; }
-  __host__ __device__ static constexpr uint32_t tP(int i) { return D == 64 ? 384 + i * 64 : i * 128; }
+  __host__ __device__ static constexpr uint32_t tP(int i) {
+    return kEarlyS ? 256 + 2 * D + i * kPCols : i * 128;
+  }
 };
 
-// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, both
-// operands fp16 or both bf16, A K-major, B K-major or MN-major, M x N.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool bf16,
+// Instruction descriptor of tcgen05.mma (kind::f16 or kind::f8f6f4): fp32
+// accumulator, A and B of one format (f16 0 / bf16 1, or e4m3 0), A K-major,
+// B K-major or MN-major, M x N.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, uint32_t fmt,
                                                   bool b_mn_major) {
   return (1u << 4)                                  // D format: f32
-         | ((bf16 ? 1u : 0u) << 7)                  // A format
-         | ((bf16 ? 1u : 0u) << 10)                 // B format
+         | (fmt << 7)                               // A format
+         | (fmt << 10)                              // B format
          | ((b_mn_major ? 1u : 0u) << 16)           // B major-ness
          | ((uint32_t)(N >> 3) << 17)               // N / 8
          | ((uint32_t)(M >> 4) << 24);              // M / 16
 }
 
-// Shared-memory matrix descriptor for the 128-byte swizzle: start address,
-// leading- and stride-dimension byte offsets, the fixed version field, and
-// the swizzle mode.
+// Shared-memory matrix descriptor: start address, leading- and stride-
+// dimension byte offsets, the fixed version field, and the swizzle mode
+// (2: 128-byte swizzle, 4: 64-byte swizzle).
 __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo,
-                                               uint32_t sbo) {
+                                               uint32_t sbo, uint64_t mode) {
   uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
   d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
   d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
+  d |= mode << 61;
   return d;
 }
 
@@ -178,13 +216,16 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity,
   }
 }
 
-template <int D, bool kBF16>
+template <int D, int T>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV,
                   const FwdParams p) {
-  using L = Layout<D>;
+  using L = Layout<D, T>;
+  using E = Elem<T>;
+  constexpr bool kF8 = E::kF8;
+  constexpr bool kOutBF16 = T != kF16;   // e4m3 inputs give a bf16 output
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -254,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kNumQ; ++i)
           for (int c = 0; c < L::kChunks; ++c)
             ptx::tma_load_3d(sbase + L::kQ + i * L::kTileBytes + c * L::kChunkBytes,
-                             &tmQ, bar(L::bQFull), c * 64, q0 + i * kBM, bh, pol_q);
+                             &tmQ, bar(L::bQFull), c * L::kChunkElems, q0 + i * kBM, bh, pol_q);
       }
       int issued = 0;
       for (int j = 0; j < nb; ++j) {
@@ -267,11 +308,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mbar_arrive_expect_tx(bar(L::bKFull + st), L::kTileBytes);
           for (int c = 0; c < L::kChunks; ++c)
             ptx::tma_load_3d(sbase + L::kK + st * L::kTileBytes + c * L::kChunkBytes,
-                             &tmK, bar(L::bKFull + st), c * 64, j * kBN, bh, pol_kv);
+                             &tmK, bar(L::bKFull + st), c * L::kChunkElems, j * kBN, bh, pol_kv);
           ptx::mbar_arrive_expect_tx(bar(L::bVFull + st), L::kTileBytes);
           for (int c = 0; c < L::kChunks; ++c)
             ptx::tma_load_3d(sbase + L::kV + st * L::kTileBytes + c * L::kChunkBytes,
-                             &tmV, bar(L::bVFull + st), c * 64, j * kBN, bh, pol_kv);
+                             &tmV, bar(L::bVFull + st), c * L::kChunkElems, j * kBN, bh, pol_kv);
         }
         issued = j + 1;
       }
@@ -290,22 +331,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================= MMA issuer
     if (nb > 0) {
       const bool leader = ptx::elect_one();
-      constexpr uint32_t idesc_s = make_idesc(kBM, kBN, kBF16, false);
-      constexpr uint32_t idesc_o = make_idesc(kBM, D, kBF16, true);
+      constexpr uint32_t idesc_s = make_idesc(kBM, kBN, E::kFmt, false);
+      constexpr uint32_t idesc_o = make_idesc(kBM, D, E::kFmt, true);
       // Descriptors are built once; stepping through a tile only adds to the
       // 14-bit start-address field (address >> 4, all smem offsets < 256 KB).
-      const uint64_t dq0 = make_sdesc(sbase + L::kQ, 16, 1024);
-      const uint64_t dk0 = make_sdesc(sbase + L::kK, 16, 1024);
-      const uint64_t dv0 = make_sdesc(sbase + L::kV, L::kChunkBytes, 1024);
+      const uint64_t dq0 = make_sdesc(sbase + L::kQ, 16, L::kSBO, L::kSwzMode);
+      const uint64_t dk0 = make_sdesc(sbase + L::kK, 16, L::kSBO, L::kSwzMode);
+      const uint64_t dv0 = make_sdesc(sbase + L::kV, L::kChunkBytes, L::kSBO, L::kSwzMode);
       // S_i = Q_i K_st^T, then a commit on s_full[i]
       auto issue_s = [&](int i, int st) {
         const uint64_t dq = dq0 + (uint64_t)((i * L::kTileBytes) >> 4);
         const uint64_t dk = dk0 + (uint64_t)((st * L::kTileBytes) >> 4);
         if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * L::kChunkBytes + (kk & 3) * 32) >> 4;
-            ptx::mma_ss(tmem + L::tS(i), dq + off, dk + off, idesc_s, kk > 0);
+          for (int kk = 0; kk < D / E::kMmaK; ++kk) {
+            // one MMA step covers 32 bytes of K: inside a swizzle row the
+            // start address moves by 32 bytes, across chunks by a chunk
+            constexpr int kStepsPerChunk = L::kSwz / 32;
+            const uint32_t off = ((kk / kStepsPerChunk) * L::kChunkBytes +
+                                  (kk % kStepsPerChunk) * 32) >> 4;
+            if constexpr (kF8)
+              ptx::mma_ss_f8(tmem + L::tS(i), dq + off, dk + off, idesc_s, kk > 0);
+            else
+              ptx::mma_ss(tmem + L::tS(i), dq + off, dk + off, idesc_s, kk > 0);
           }
           ptx::mma_commit(bar(L::bSFull + i));
         }
@@ -315,10 +363,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dv = dv0 + (uint64_t)((st * L::kTileBytes) >> 4);
         if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            ptx::mma_ts(tmem + L::tO(i), tmem + L::tP(i) + kk * 8,
-                        dv + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
-                        (acc || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBN / E::kMmaK; ++kk) {
+            // K step of kMmaK keys: 8 TMEM columns of P, kMmaK swizzle rows of V
+            const uint64_t dvk = dv + (uint64_t)((kk * E::kMmaK * L::kSwz) >> 4);
+            if constexpr (kF8)
+              ptx::mma_ts_f8(tmem + L::tO(i), tmem + L::tP(i) + kk * 8, dvk, idesc_o,
+                             (acc || kk > 0) ? 1u : 0u);
+            else
+              ptx::mma_ts(tmem + L::tO(i), tmem + L::tP(i) + kk * 8, dvk, idesc_o,
+                          (acc || kk > 0) ? 1u : 0u);
           }
           ptx::mma_commit(bar(L::bODone + i));
         }
@@ -437,14 +490,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2 nm2 = make_float2(-m_use, -m_use);
       float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                       make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      uint32_t pk[kBN / 2];
+      // P in the MMA's input type: two 16-bit or four e4m3 values a word
+      uint32_t pk[L::kPCols];
 #pragma unroll
-      for (int cc = 0; cc < kBN; cc += 2) {
-        const float2 x = __ffma2_rn(make_float2(sf[cc], sf[cc + 1]), c2, nm2);
-        const float p0 = ptx::ex2_approx(x.x);
-        const float p1 = ptx::ex2_approx(x.y);
+      for (int cc = 0; cc < kBN; cc += 4) {
+        const float2 x0 = __ffma2_rn(make_float2(sf[cc], sf[cc + 1]), c2, nm2);
+        const float2 x1 = __ffma2_rn(make_float2(sf[cc + 2], sf[cc + 3]), c2, nm2);
+        const float p0 = ptx::ex2_approx(x0.x);
+        const float p1 = ptx::ex2_approx(x0.y);
+        const float p2 = ptx::ex2_approx(x1.x);
+        const float p3 = ptx::ex2_approx(x1.y);
         rs[(cc >> 1) & 3] = __fadd2_rn(rs[(cc >> 1) & 3], make_float2(p0, p1));
-        pk[cc / 2] = kBF16 ? ptx::pack_bf16(p0, p1) : ptx::pack_f16(p0, p1);
+        rs[((cc >> 1) + 1) & 3] = __fadd2_rn(rs[((cc >> 1) + 1) & 3], make_float2(p2, p3));
+        if constexpr (kF8) {
+          pk[cc / 4] = ptx::pack_e4m3x4(p0, p1, p2, p3);
+        } else if constexpr (T == kBF16) {
+          pk[cc / 2] = ptx::pack_bf16(p0, p1);
+          pk[cc / 2 + 1] = ptx::pack_bf16(p2, p3);
+        } else {
+          pk[cc / 2] = ptx::pack_f16(p0, p1);
+          pk[cc / 2 + 1] = ptx::pack_f16(p2, p3);
+        }
       }
       // O_i += P_i V_{j-1} must be complete before P_i is overwritten and
       // before O_i is rescaled.
@@ -453,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
       }
 #pragma unroll
-      for (int cc = 0; cc < kBN / 2; cc += 32)
+      for (int cc = 0; cc < L::kPCols; cc += 32)
         ptx::tmem_st32(tP + cc, *reinterpret_cast<uint32_t(*)[32]>(&pk[cc]));
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         const float2 a2 = make_float2(alpha, alpha);
@@ -487,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       ptx::tc_fence_after();
       const bool valid = row < p.Nq;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? p.o_scale / l : 0.f;
       const size_t orow = (size_t)bh * (size_t)p.Nq + (size_t)row;
       uint16_t *optr = reinterpret_cast<uint16_t *>(p.o) + orow * D;
 #pragma unroll
@@ -506,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 16; ++t) {
           const float a = __uint_as_float(o[2 * t]) * inv;
           const float b = __uint_as_float(o[2 * t + 1]) * inv;
-          w[t] = kBF16 ? ptx::pack_bf16(a, b) : ptx::pack_f16(a, b);
+          w[t] = kOutBF16 ? ptx::pack_bf16(a, b) : ptx::pack_f16(a, b);
         }
         if (valid) {
           uint4 *dst = reinterpret_cast<uint4 *>(optr + cc * 32);

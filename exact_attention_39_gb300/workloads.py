@@ -18,7 +18,11 @@ import math
 
 import torch
 
-DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16}
+DTYPES = {"fp16": torch.float16, "bf16": torch.bfloat16,
+          "e4m3": torch.float8_e4m3fn}
+# Per-tensor descale of the e4m3 inputs: x is stored as round(x / E4M3_DESCALE),
+# which keeps N(0, 1) data (|x| < 14) inside e4m3's range (448).
+E4M3_DESCALE = 1.0 / 32.0
 
 
 @dataclass(frozen=True)
@@ -28,7 +32,7 @@ class Workload:
     H: int
     N: int
     d: int
-    dtype: str                 # "fp16" | "bf16"
+    dtype: str                 # "fp16" | "bf16" | "e4m3"
     causal: bool
     seed: int = 0
     q_mult: float = 1.0        # exact power of two applied to q
@@ -54,11 +58,12 @@ class Workload:
         return f / 2.0 if self.causal else f
 
     def hbm_bytes(self):
-        """Algorithmic HBM bytes: read Q, K, V and write O once (2 B each)
-        plus the fp32 LSE."""
-        e = 2
+        """Algorithmic HBM bytes: read Q, K, V once at their element size,
+        write O once (2 B; bf16 for e4m3 inputs) and the fp32 LSE."""
+        e = 1 if self.dtype == "e4m3" else 2     # O is bf16 for e4m3 inputs
         bh = self.B * self.H
-        return bh * ((self.N * 2 + self.n_keys * 2) * self.d * e + 4 * self.N)
+        return bh * ((self.N + 2 * self.n_keys) * self.d * e
+                     + self.N * self.d * 2 + 4 * self.N)
 
     def kv_bytes(self):
         """Bytes of K and V together (fp16/bf16)."""
@@ -83,6 +88,17 @@ N8192_CAUSAL = N8192.with_(name="b8h32n8192d64_bf16_causal", causal=True)
 LONG = Workload("b1h32n32768d128_bf16_causal", 1, 32, 32768, 128, "bf16",
                 True, seed=0, in_mult=0.5)
 SWEEP_N = (512, 1024, 2048, 4096, 8192)
+
+
+N8192_E4M3 = N8192.with_(name="b8h32n8192d64_e4m3", dtype="e4m3")
+N8192_E4M3_CAUSAL = N8192_E4M3.with_(name="b8h32n8192d64_e4m3_causal", causal=True)
+
+
+def dequantized(t, dtype):
+    """The real values an input tensor stands for, in float64."""
+    if dtype == "e4m3":
+        return t.double() * E4M3_DESCALE
+    return t.double()
 
 
 def sweep(causal=False):
@@ -111,7 +127,11 @@ def make_inputs(w, device="cpu"):
         q.mul_(w.in_mult)
         k.mul_(w.in_mult)
         v.mul_(w.in_mult)
-    out = tuple(t.to(dt) for t in (q, k, v))
+    if w.dtype == "e4m3":
+        # saturating quantisation (e4m3 has no infinity; out of range is NaN)
+        out = tuple((t / E4M3_DESCALE).clamp(-448.0, 448.0).to(dt) for t in (q, k, v))
+    else:
+        out = tuple(t.to(dt) for t in (q, k, v))
     if device != "cpu":
         out = tuple(t.to(device) for t in out)
     return out

@@ -107,6 +107,32 @@ FA_API fa_status fa_fwd_qk(const void *q, const void *k, const void *v,
                            int d, int causal, float scale, fa_dtype dtype,
                            fa_stream_t stream);
 
+/*
+ * fa_fwd_fp8 -- the forward pass on FP8 (e4m3) inputs, with a bf16 output.
+ *
+ * The FP8 variant is the pages' FlashAttention-3 FP8 column on H100 and
+ * its "FP8 precision in commercial use" outlook (baguaai.com benchmarks
+ * page, "H100 80GB" table; zzycbzc.com/news/393333, "推理优化的未来方向",
+ * item 2).  Both products run on the tcgen05 tensor cores in kind::f8f6f4
+ * with fp32 accumulation.
+ *
+ *   q, k, v : [B, H, Nq|Nk, d] e4m3 (one byte each), 16-byte aligned.  The
+ *             real values are q * q_descale, k * k_descale, v * v_descale
+ *             (per-tensor descales, finite and > 0).
+ *   o       : [B, H, Nq, d] bf16;  lse : [B, H, Nq] fp32 (natural log of the
+ *             scaled logits of the real values).
+ *   scale, causal, B, H, Nq, Nk, d, stream : as fa_fwd_qk.
+ * P (the softmax probabilities, at most 256 under the rescale rule) is
+ * rounded to e4m3 for the second product; the row sums use the fp32
+ * probabilities.  Errors as fa_fwd_qk, plus FA_ERR_SCALE for a descale that
+ * is not finite and positive.
+ */
+FA_API fa_status fa_fwd_fp8(const void *q, const void *k, const void *v,
+                            void *o, float *lse, int B, int H, int Nq, int Nk,
+                            int d, int causal, float scale, float q_descale,
+                            float k_descale, float v_descale,
+                            fa_stream_t stream);
+
 /* A static, human-readable description of a status code. */
 FA_API const char *fa_status_string(fa_status status);
 
