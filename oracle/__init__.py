@@ -56,6 +56,11 @@ def _load():
             dp, dp, dp, ctypes.c_long, ctypes.c_long, ctypes.c_long,
             ctypes.c_int, ctypes.c_double, ctypes.c_long, dp]
         lib.fa_oracle_row_weights.restype = ctypes.c_long
+        lib.fa_oracle_bwd.argtypes = [
+            dp, dp, dp, dp, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+            ctypes.c_long, ctypes.c_int, ctypes.c_double, dp, dp, dp,
+            ctypes.c_int]
+        lib.fa_oracle_bwd.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -108,6 +113,29 @@ def attention_fwd(q, k, v, scale, causal, rows=None, nthreads=None):
     if rc != 0:
         raise ValueError("fa_oracle_fwd rejected its arguments")
     return o, lse
+
+
+def attention_bwd(q, k, v, dout, scale, causal, nthreads=None):
+    """Gradients (dQ, dK, dV) of L = sum(O * dout) for O = attention(q, k, v),
+    in fp64, shapes as attention_fwd (dout like q)."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    lead = q.shape[:-2]
+    nq, d = q.shape[-2], q.shape[-1]
+    nk = k.shape[-2]
+    if (k.shape[:-2] != lead or v.shape != k.shape or k.shape[-1] != d
+            or dout.shape != q.shape):
+        raise ValueError("q, k, v, dout shapes disagree")
+    bh = int(np.prod(lead)) if lead else 1
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    nt = default_threads() if nthreads is None else int(nthreads)
+    rc = _load().fa_oracle_bwd(_dptr(q), _dptr(k), _dptr(v), _dptr(dout), bh,
+                               nq, nk, d, int(bool(causal)), float(scale),
+                               _dptr(dq), _dptr(dk), _dptr(dv), nt)
+    if rc != 0:
+        raise ValueError("fa_oracle_bwd rejected its arguments")
+    return dq, dk, dv
 
 
 def row_weights(q, k, v, scale, causal, i):

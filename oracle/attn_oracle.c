@@ -178,6 +178,119 @@ int fa_oracle_fwd(const double *q, const double *k, const double *v,
 }
 
 /*
+ * Backward of the same attention, from the plain definition.  With
+ * P = softmax(scale * Q K^T [mask]) and O = P V, for an upstream gradient
+ * dO of O (the loss L = sum(O .* dO)):
+ *   dV = P^T dO
+ *   dP = dO V^T,   D_i = sum_t dO_it O_it
+ *   dS = P .* (dP - D)          (the softmax Jacobian applied to dP)
+ *   dQ = scale * dS K,   dK = scale * dS^T Q
+ * computed row by row: each query row's P is built with the forward row
+ * routine, dQ_i is finished at once, and dK, dV accumulate over the rows.
+ * Rows are split into one chunk per thread, each with its own dK/dV partial
+ * sums that are added at the end in chunk order (the result is the same for
+ * a given thread count).
+ */
+typedef struct {
+    const double *q, *k, *v, *dout;
+    long Nq, Nk, d;
+    int causal;
+    double scale;
+    long row0, row1;
+    double *dq;               /* rows row0..row1 of dQ for this head */
+    double *dk, *dv;          /* chunk-private [Nk, d] partial sums  */
+} bwd_chunk;
+
+static void *bwd_worker(void *arg)
+{
+    bwd_chunk *c = (bwd_chunk *)arg;
+    const long d = c->d, Nk = c->Nk;
+    double *w = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+    double *o_row = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!w || !o_row) { free(w); free(o_row); return NULL; }
+    for (long i = c->row0; i < c->row1; ++i) {
+        const double *qi = c->q + i * d, *gi = c->dout + i * d;
+        double lse;
+        long n = attn_row(qi, c->k, c->v, i, c->Nq, Nk, d, c->causal, c->scale,
+                          o_row, &lse, w);
+        double *dqi = c->dq + (i - c->row0) * d;
+        for (long t = 0; t < d; ++t) dqi[t] = 0.0;
+        if (n == 0) continue;
+        double l = 0.0;
+        for (long j = 0; j < n; ++j) l += w[j];
+        double Di = 0.0;
+        for (long t = 0; t < d; ++t) Di += gi[t] * o_row[t];
+        for (long j = 0; j < n; ++j) {
+            const double pj = w[j] / l;
+            const double *vj = c->v + j * d, *kj = c->k + j * d;
+            double dpj = 0.0;
+            for (long t = 0; t < d; ++t) dpj += gi[t] * vj[t];
+            const double dsj = pj * (dpj - Di);
+            for (long t = 0; t < d; ++t) {
+                c->dv[j * d + t] += pj * gi[t];
+                c->dk[j * d + t] += c->scale * dsj * qi[t];
+                dqi[t] += c->scale * dsj * kj[t];
+            }
+        }
+    }
+    free(w);
+    free(o_row);
+    return NULL;
+}
+
+/*
+ * fa_oracle_bwd: gradients for BH independent problems.
+ *   q, dout: [BH, Nq, d]; k, v: [BH, Nk, d]  ->  dq [BH, Nq, d],
+ *   dk, dv [BH, Nk, d].  Returns 0, or -1 on bad arguments / no memory.
+ */
+int fa_oracle_bwd(const double *q, const double *k, const double *v,
+                  const double *dout, long BH, long Nq, long Nk, long d,
+                  int causal, double scale, double *dq, double *dk, double *dv,
+                  int nthreads)
+{
+    if (!q || !k || !v || !dout || !dq || !dk || !dv) return -1;
+    if (BH < 0 || Nq < 0 || Nk < 0 || d <= 0) return -1;
+    if (nthreads < 1) nthreads = 1;
+    const long nchunks = nthreads;
+    bwd_chunk *ch = (bwd_chunk *)malloc(sizeof(bwd_chunk) * (size_t)nchunks);
+    double *part = (double *)calloc((size_t)(2 * nchunks * (Nk > 0 ? Nk : 1) * d),
+                                    sizeof(double));
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nchunks);
+    if (!ch || !part || !tid) { free(ch); free(part); free(tid); return -1; }
+    for (long h = 0; h < BH; ++h) {
+        const long per = (Nq + nchunks - 1) / nchunks;
+        for (long t = 0; t < nchunks; ++t) {
+            bwd_chunk *c = &ch[t];
+            c->q = q + h * Nq * d; c->dout = dout + h * Nq * d;
+            c->k = k + h * Nk * d; c->v = v + h * Nk * d;
+            c->Nq = Nq; c->Nk = Nk; c->d = d; c->causal = causal; c->scale = scale;
+            c->row0 = t * per < Nq ? t * per : Nq;
+            c->row1 = (t + 1) * per < Nq ? (t + 1) * per : Nq;
+            c->dq = dq + (h * Nq + c->row0) * d;
+            c->dk = part + (2 * t) * Nk * d;
+            c->dv = part + (2 * t + 1) * Nk * d;
+            memset(c->dk, 0, sizeof(double) * (size_t)(2 * Nk * d));
+        }
+        int started = 0;
+        for (; started < nchunks; ++started)
+            if (pthread_create(&tid[started], NULL, bwd_worker, &ch[started]) != 0) break;
+        for (long t = started; t < nchunks; ++t) bwd_worker(&ch[t]);
+        for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+        double *dkh = dk + h * Nk * d, *dvh = dv + h * Nk * d;
+        for (long e = 0; e < Nk * d; ++e) { dkh[e] = 0.0; dvh[e] = 0.0; }
+        for (long t = 0; t < nchunks; ++t)
+            for (long e = 0; e < Nk * d; ++e) {
+                dkh[e] += ch[t].dk[e];
+                dvh[e] += ch[t].dv[e];
+            }
+    }
+    free(ch);
+    free(part);
+    free(tid);
+    return 0;
+}
+
+/*
  * The normalised softmax weights p_ij = exp(s_ij - m_i) / l_i of one query
  * row i of one head, from the same row routine the forward uses.
  * p: Nk doubles; entries for masked keys are set to 0.

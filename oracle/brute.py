@@ -47,3 +47,22 @@ def attention_brute(q, k, v, scale, causal):
     o = [[math.fsum(p[i][j] * v[j][t] for j in range(nk)) for t in range(d)]
          for i in range(nq)]
     return o, lse, p
+
+
+def attention_brute_bwd(q, k, v, dout, scale, causal):
+    """Unfused backward (tiny shapes): full P, dP and dS matrices.
+    Returns dQ, dK, dV as nested lists."""
+    o, _, p = attention_brute(q, k, v, scale, causal)
+    nq, nk = len(q), len(k)
+    d = len(q[0]) if nq else 0
+    dv = [[math.fsum(p[i][j] * dout[i][t] for i in range(nq)) for t in range(d)]
+          for j in range(nk)]
+    dp = [[math.fsum(dout[i][t] * v[j][t] for t in range(d)) for j in range(nk)]
+          for i in range(nq)]
+    dd = [math.fsum(dout[i][t] * o[i][t] for t in range(d)) for i in range(nq)]
+    ds = [[p[i][j] * (dp[i][j] - dd[i]) for j in range(nk)] for i in range(nq)]
+    dq = [[scale * math.fsum(ds[i][j] * k[j][t] for j in range(nk)) for t in range(d)]
+          for i in range(nq)]
+    dk = [[scale * math.fsum(ds[i][j] * q[i][t] for i in range(nq)) for t in range(d)]
+          for j in range(nk)]
+    return dq, dk, dv
