@@ -8,7 +8,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB_NAME = "libfa_sm103.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 SOURCES = ["fa_api.cu"]
-DEPS = ["fa_fwd_kernel.cuh", "ptx.cuh"]
+DEPS = ["fa_fwd_kernel.cuh", "fa_bwd_kernel.cuh", "ptx.cuh"]
 HEADERS = ["fa.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

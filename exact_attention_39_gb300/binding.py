@@ -22,11 +22,12 @@ FA_ERR_ALIGN = 5
 FA_ERR_SCALE = 6
 FA_ERR_CUDA = 7
 FA_ERR_DEVICE_TIMEOUT = 8
+FA_ERR_WORKSPACE = 9
 FA_FP16 = 0
 FA_BF16 = 1
 
-EXPORTED = ("fa_fwd", "fa_fwd_qk", "fa_fwd_fp8", "fa_status_string",
-            "fa_last_device_error", "fa_version")
+EXPORTED = ("fa_fwd", "fa_fwd_qk", "fa_fwd_fp8", "fa_bwd", "fa_bwd_workspace_bytes",
+            "fa_status_string", "fa_last_device_error", "fa_version")
 
 _lib = None
 
@@ -55,6 +56,12 @@ def load_library(path=None):
     lib.fa_fwd_qk.restype = i
     lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, f, f, vp]
     lib.fa_fwd_fp8.restype = i
+    sz = ctypes.c_size_t
+    lib.fa_bwd_workspace_bytes.argtypes = [i, i, i]
+    lib.fa_bwd_workspace_bytes.restype = sz
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i,
+                           i, f, i, vp]
+    lib.fa_bwd.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_device_error.argtypes = [vp]
@@ -192,6 +199,59 @@ def fwd_fp8(q, k, v, q_descale, k_descale, v_descale, causal=False,
                               causal, scale, q_descale, k_descale, v_descale,
                               _stream_handle(stream)))
     return out, lse
+
+
+def bwd_workspace_bytes(B, H, N):
+    return int(load_library().fa_bwd_workspace_bytes(int(B), int(H), int(N)))
+
+
+def fa_bwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, do_ptr, lse_ptr, dq_ptr, dk_ptr,
+               dv_ptr, ws_ptr, ws_bytes, B, H, N, d, causal, scale, dtype_code,
+               stream_handle):
+    """The C call of the backward; returns the status."""
+    return load_library().fa_bwd(q_ptr, k_ptr, v_ptr, o_ptr, do_ptr, lse_ptr,
+                                 dq_ptr, dk_ptr, dv_ptr, ws_ptr, int(ws_bytes),
+                                 int(B), int(H), int(N), int(d),
+                                 int(bool(causal)), float(scale),
+                                 int(dtype_code), stream_handle)
+
+
+def bwd(q, k, v, o, lse, dout, causal=False, scale=None, dq=None, dk=None,
+        dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of the attention forward for the upstream
+    gradient ``dout`` of ``o``.  All [B, H, N, d] CUDA tensors of one dtype
+    (``lse`` [B, H, N] float32, as ``fwd`` returned them).  ``workspace``
+    (a CUDA uint8 tensor of at least ``bwd_workspace_bytes`` bytes) is
+    allocated when not given."""
+    if q.dim() != 4 or any(t.shape != q.shape for t in (k, v, o, dout)):
+        raise ValueError("q, k, v, o, dout must all be [B, H, N, d]")
+    if not (q.dtype == k.dtype == v.dtype == o.dtype == dout.dtype):
+        raise TypeError("q, k, v, o, dout must share one dtype")
+    code = _dtype_code(q)
+    for t in (q, k, v, o, dout, lse):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    B, H, N, d = q.shape
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32:
+        raise ValueError("lse must be a float32 [B, H, N] tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t in (dq, dk, dv):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError("dq, dk, dv must be contiguous tensors like q")
+    need = bwd_workspace_bytes(B, H, N)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        _check(fa_bwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                          dout.data_ptr(), lse.data_ptr(), dq.data_ptr(),
+                          dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+                          workspace.numel() * workspace.element_size(), B, H, N,
+                          d, causal, scale, code, _stream_handle(stream)))
+    return dq, dk, dv
 
 
 def fwd_host(q_h, k_h, v_h, q_d, k_d, v_d, o_d, lse_d, o_h, lse_h,

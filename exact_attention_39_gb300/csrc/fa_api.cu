@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_bwd_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
@@ -62,6 +63,23 @@ fa_status ensure_ready(int dev) {
   for (int t = 0; t < 6; ++t)
     if (cudaFuncSetAttribute(kernels[t], cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem[t]) != cudaSuccess)
+      return FA_ERR_CUDA;
+  const void *bwd_kernels[8] = {
+      reinterpret_cast<void *>(&fa_bwd_dq_kernel<64, kF16>),
+      reinterpret_cast<void *>(&fa_bwd_dq_kernel<64, kBF16>),
+      reinterpret_cast<void *>(&fa_bwd_dq_kernel<128, kF16>),
+      reinterpret_cast<void *>(&fa_bwd_dq_kernel<128, kBF16>),
+      reinterpret_cast<void *>(&fa_bwd_dkdv_kernel<64, kF16>),
+      reinterpret_cast<void *>(&fa_bwd_dkdv_kernel<64, kBF16>),
+      reinterpret_cast<void *>(&fa_bwd_dkdv_kernel<128, kF16>),
+      reinterpret_cast<void *>(&fa_bwd_dkdv_kernel<128, kBF16>)};
+  const int bwd_smem[8] = {BwdQLayout<64, kF16>::kAlloc, BwdQLayout<64, kBF16>::kAlloc,
+                           BwdQLayout<128, kF16>::kAlloc, BwdQLayout<128, kBF16>::kAlloc,
+                           BwdKVLayout<64, kF16>::kAlloc, BwdKVLayout<64, kBF16>::kAlloc,
+                           BwdKVLayout<128, kF16>::kAlloc, BwdKVLayout<128, kBF16>::kAlloc};
+  for (int t = 0; t < 8; ++t)
+    if (cudaFuncSetAttribute(bwd_kernels[t], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bwd_smem[t]) != cudaSuccess)
       return FA_ERR_CUDA;
   void *addr = nullptr;
   if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess || !addr)
@@ -117,6 +135,32 @@ fa_status run(const void *q, const void *k, const void *v, FwdParams p,
 }
 
 bool aligned(const void *p, uintptr_t a);
+
+// Encodes the four maps and launches the three backward kernels.
+template <int D, int T>
+fa_status run_bwd(const void *q, const void *k, const void *v, const void *dout,
+                  const BwdParams &p, long long bh, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_map<D, T>(&mq, q, p.Nq, bh) || !encode_map<D, T>(&mk, k, p.Nk, bh) ||
+      !encode_map<D, T>(&mv, v, p.Nk, bh) || !encode_map<D, T>(&mdo, dout, p.Nq, bh))
+    return FA_ERR_CUDA;
+  const long long rows = bh * (long long)p.Nq;
+  const long long threads = rows * 8;
+  fa_bwd_dot_kernel<D, T><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(p, rows);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kBwdThreads, 1, 1);
+  cfg.stream = stream;
+  cfg.gridDim = dim3((unsigned)(bh * p.n_qblk), 1, 1);
+  cfg.dynamicSmemBytes = BwdQLayout<D, T>::kAlloc;
+  if (cudaLaunchKernelEx(&cfg, fa_bwd_dq_kernel<D, T>, mq, mk, mv, mdo, p) != cudaSuccess)
+    return FA_ERR_CUDA;
+  cfg.gridDim = dim3((unsigned)(bh * p.n_kblk), 1, 1);
+  cfg.dynamicSmemBytes = BwdKVLayout<D, T>::kAlloc;
+  if (cudaLaunchKernelEx(&cfg, fa_bwd_dkdv_kernel<D, T>, mq, mk, mv, mdo, p) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
 
 // Shared argument checks and set-up of fa_fwd_qk and fa_fwd_fp8.  Returns
 // FA_OK with *launch false for an empty problem.
@@ -227,6 +271,63 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o,
   return fa_fwd_qk(q, k, v, o, lse, B, H, N, N, d, causal, scale, dtype, stream);
 }
 
+size_t fa_bwd_workspace_bytes(int B, int H, int N) {
+  if (B <= 0 || H <= 0 || N <= 0) return 0;
+  const size_t bytes = (size_t)B * (size_t)H * (size_t)N * sizeof(float);
+  return (bytes + 255) & ~(size_t)255;
+}
+
+fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
+                 const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                 void *workspace, size_t workspace_bytes, int B, int H, int N,
+                 int d, int causal, float scale, fa_dtype dtype,
+                 fa_stream_t stream) {
+  using namespace fa;
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+  if (B == 0 || H == 0 || N == 0) return FA_OK;   // empty problem
+  // every host-side check before the first CUDA call
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_NULL;
+  if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
+    return FA_ERR_ALIGN;
+  if (!workspace || !aligned(workspace, 16) ||
+      workspace_bytes < fa_bwd_workspace_bytes(B, H, N))
+    return FA_ERR_WORKSPACE;
+  long long bh = 0, units = 0;
+  int dev = 0;
+  bool launch = false;
+  fa_status st = prepare(q, k, v, o, lse, B, H, N, N, d, scale, &bh, &units,
+                         &dev, &launch);
+  if (st != FA_OK || !launch) return st;
+  BwdParams p;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.dsum = static_cast<float *>(workspace);
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.Nq = N;
+  p.Nk = N;
+  p.n_qblk = (N + kBM - 1) / kBM;
+  p.n_kblk = (N + kBN - 1) / kBN;
+  p.causal = causal ? 1 : 0;
+  p.c = (float)((double)scale * 1.4426950408889634);
+  p.scale = scale;
+  p.timeout_ns = kTimeoutNs;
+  p.status = g_status_ptr[dev];
+  if (bh * (long long)p.n_kblk > (1ll << 31) - 1) return FA_ERR_SHAPE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool bf16 = dtype == FA_BF16;
+  if (d == 64)
+    return bf16 ? run_bwd<64, kBF16>(q, k, v, dout, p, bh, s)
+                : run_bwd<64, kF16>(q, k, v, dout, p, bh, s);
+  return bf16 ? run_bwd<128, kBF16>(q, k, v, dout, p, bh, s)
+              : run_bwd<128, kF16>(q, k, v, dout, p, bh, s);
+}
+
 const char *fa_status_string(fa_status status) {
   switch (status) {
     case FA_OK: return "ok";
@@ -238,6 +339,7 @@ const char *fa_status_string(fa_status status) {
     case FA_ERR_SCALE: return "scale must be finite and positive";
     case FA_ERR_CUDA: return "CUDA error (call failed, or device is not sm_103)";
     case FA_ERR_DEVICE_TIMEOUT: return "a bounded on-device wait timed out";
+    case FA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
   }
   return "unknown status";
 }

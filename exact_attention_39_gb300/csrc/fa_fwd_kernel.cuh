@@ -175,10 +175,12 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo,
 
 // A bounded wait on an mbarrier phase.  Gives up when the CTA's abort flag is
 // set or after timeout_ns of global time; on a timeout it sets the abort flag
-// and records the timeout in the device status word.
+// and records the timeout in the device status word.  (P: any parameter
+// block with timeout_ns and status.)
+template <class P>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
                                            volatile int *abort_flag,
-                                           const FwdParams &p) {
+                                           const P &p) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -195,17 +197,19 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
 }
 
 // wait_phase executed by all 32 lanes of a warp, with one warp-wide verdict.
+template <class P>
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
                                           volatile int *abort_flag,
-                                          const FwdParams &p) {
+                                          const P &p) {
   const bool ok = wait_phase(bar, parity, abort_flag, p);
   return __all_sync(0xffffffffu, ok);
 }
 
 // A wait used only while draining on the way out: bounded by the timeout
 // alone (it must not give up just because the CTA is aborting).
+template <class P>
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity,
-                                           const FwdParams &p) {
+                                           const P &p) {
   const uint64_t t0 = ptx::globaltimer_ns();
   for (;;) {
     if (ptx::mbar_try_wait(bar, parity)) return true;

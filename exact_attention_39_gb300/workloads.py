@@ -137,6 +137,14 @@ def make_inputs(w, device="cpu"):
     return out
 
 
+def make_upstream_grad(w, seed_offset=1000):
+    """dO for the backward: i.i.d. N(0, 1) like q, from its own seed."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(w.seed) + seed_offset)
+    t = torch.randn((w.B, w.H, w.N, w.d), generator=g, dtype=torch.float32)
+    return t.to(DTYPES[w.dtype])
+
+
 def sample_heads(w, count, seed=1234):
     """``count`` distinct (b, h) pairs, drawn without replacement."""
     g = torch.Generator(device="cpu")

@@ -24,6 +24,8 @@
 #ifndef FA_H_
 #define FA_H_
 
+#include <stddef.h>
+
 #if defined(__GNUC__)
 #define FA_API __attribute__((visibility("default")))
 #else
@@ -49,8 +51,9 @@ typedef enum {
     FA_ERR_SCALE = 6,          /* scale is not finite and positive           */
     FA_ERR_CUDA = 7,           /* a CUDA runtime/driver call failed, or the
                                   device is not sm_103 / lacks resources     */
-    FA_ERR_DEVICE_TIMEOUT = 8  /* a bounded on-device wait ran out; the
+    FA_ERR_DEVICE_TIMEOUT = 8, /* a bounded on-device wait ran out; the
                                   outputs of that launch are undefined      */
+    FA_ERR_WORKSPACE = 9       /* workspace missing, misaligned or too small */
 } fa_status;
 
 typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype;
@@ -132,6 +135,36 @@ FA_API fa_status fa_fwd_fp8(const void *q, const void *k, const void *v,
                             int d, int causal, float scale, float q_descale,
                             float k_descale, float v_descale,
                             fa_stream_t stream);
+
+/*
+ * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs for
+ * B*H*N query rows (one fp32 per row, rounded up to 256 bytes).
+ */
+FA_API size_t fa_bwd_workspace_bytes(int B, int H, int N);
+
+/*
+ * fa_bwd -- gradients of the attention forward (fa_fwd with the same
+ * arguments) for an upstream gradient dout of O.
+ *
+ *   q, k, v, o, dout : [B, H, N, d] dtype, o and lse as fa_fwd produced them.
+ *   lse              : [B, H, N] fp32.
+ *   dq, dk, dv       : [B, H, N, d] dtype (written):
+ *       dV = P^T dout,  dS = P .* (dout V^T - rowsum(dout .* o)),
+ *       dQ = scale * dS K,  dK = scale * dS^T Q,  P = exp(scale Q K^T - lse).
+ *   workspace        : caller-owned device memory of at least
+ *                      fa_bwd_workspace_bytes(B, H, N) bytes, 16-byte
+ *                      aligned; its contents on entry do not matter, and
+ *                      calls that run concurrently need separate workspaces.
+ * P is recomputed from q, k and lse, never stored.  Three kernels are
+ * enqueued on `stream` (row sums, dQ, then dK and dV).  Errors as fa_fwd,
+ * plus FA_ERR_WORKSPACE.  d is 64 or 128; dtype FA_FP16 or FA_BF16.
+ */
+FA_API fa_status fa_bwd(const void *q, const void *k, const void *v,
+                        const void *o, const void *dout, const float *lse,
+                        void *dq, void *dk, void *dv, void *workspace,
+                        size_t workspace_bytes, int B, int H, int N, int d,
+                        int causal, float scale, fa_dtype dtype,
+                        fa_stream_t stream);
 
 /* A static, human-readable description of a status code. */
 FA_API const char *fa_status_string(fa_status status);
