@@ -27,7 +27,9 @@ FA_FP16 = 0
 FA_BF16 = 1
 
 EXPORTED = ("fa_fwd", "fa_fwd_qk", "fa_fwd_fp8", "fa_bwd", "fa_bwd_workspace_bytes",
-            "fa_status_string", "fa_last_device_error", "fa_version")
+            "fa_bwd_noalloc", "fa_status_string", "fa_last_device_error",
+            "fa_version")
+FA_BWD_NOALLOC_MAX_ROWS = 1 << 21
 
 _lib = None
 
@@ -62,6 +64,9 @@ def load_library(path=None):
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i,
                            i, f, i, vp]
     lib.fa_bwd.restype = i
+    lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i,
+                                   i, f, i, vp]
+    lib.fa_bwd_noalloc.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_device_error.argtypes = [vp]
@@ -214,6 +219,19 @@ def fa_bwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, do_ptr, lse_ptr, dq_ptr, dk_ptr,
                                  int(B), int(H), int(N), int(d),
                                  int(bool(causal)), float(scale),
                                  int(dtype_code), stream_handle)
+
+
+def fa_bwd_noalloc_raw(q_ptr, k_ptr, v_ptr, o_ptr, do_ptr, lse_ptr, dq_ptr,
+                       dk_ptr, dv_ptr, B, H, N, d, causal, scale, dtype_code,
+                       stream_handle):
+    """The C call of the backward that uses the library's static scratch
+    instead of a workspace (for callers that cannot allocate); returns the
+    status."""
+    return load_library().fa_bwd_noalloc(q_ptr, k_ptr, v_ptr, o_ptr, do_ptr,
+                                         lse_ptr, dq_ptr, dk_ptr, dv_ptr,
+                                         int(B), int(H), int(N), int(d),
+                                         int(bool(causal)), float(scale),
+                                         int(dtype_code), stream_handle)
 
 
 def bwd(q, k, v, o, lse, dout, causal=False, scale=None, dq=None, dk=None,

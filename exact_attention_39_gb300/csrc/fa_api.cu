@@ -365,3 +365,57 @@ fa_status fa_last_device_error(fa_stream_t stream) {
 int fa_version(void) { return 100; }
 
 }  // extern "C"
+
+namespace fa {
+namespace {
+
+// Row sums D of fa_bwd_noalloc: static device memory (one copy on every
+// device that loads the library), shared by all calls.
+constexpr long long kNoAllocMaxRows = FA_BWD_NOALLOC_MAX_ROWS;
+static __device__ __align__(256) float g_noalloc_dsum[kNoAllocMaxRows];
+
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// The array's device address for device `dev` (current), looked up once.
+fa_status noalloc_scratch(int dev, void **out) {
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_dsum) != cudaSuccess || !ptr)
+      return FA_ERR_CUDA;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v,
+                         const void *o, const void *dout, const float *lse,
+                         void *dq, void *dk, void *dv, int B, int H, int N,
+                         int d, int causal, float scale, fa_dtype dtype,
+                         fa_stream_t stream) {
+  using namespace fa;
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_SHAPE;
+  if (B == 0 || H == 0 || N == 0)   // empty problem: fa_bwd's checks, no scratch
+    return fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, nullptr, 0, B, H, N, d,
+                  causal, scale, dtype, stream);
+  if ((long long)B * (long long)H * (long long)N > kNoAllocMaxRows)
+    return FA_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  void *scratch = nullptr;
+  const fa_status st = noalloc_scratch(dev, &scratch);
+  if (st != FA_OK) return st;
+  return fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, scratch,
+                (size_t)kNoAllocMaxRows * sizeof(float), B, H, N, d, causal,
+                scale, dtype, stream);
+}
+
+}  // extern "C"

@@ -166,6 +166,38 @@ FA_API fa_status fa_bwd(const void *q, const void *k, const void *v,
                         int causal, float scale, fa_dtype dtype,
                         fa_stream_t stream);
 
+/*
+ * fa_bwd_noalloc -- fa_bwd for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart of this entry point.  It exists for code
+ * that must not call cudaMalloc or an allocator of its own: for instance a
+ * plug-in running inside a host program that owns every device allocation,
+ * or a latency-bound loop that may not pay for an allocation.  fa_bwd needs
+ * a workspace of fa_bwd_workspace_bytes(B, H, N) bytes; this variant uses a
+ * fixed array in the library's static device memory instead, so it takes no
+ * workspace argument and allocates nothing.
+ *
+ * Limit: B * H * N <= FA_BWD_NOALLOC_MAX_ROWS (2^21, one fp32 per query
+ * row: 8 MiB held on every device that loads the library, until the
+ * process exits).  Larger problems return FA_ERR_WORKSPACE without touching
+ * the device; use fa_bwd with a workspace for them.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call shares the one array and leaves its contents behind;
+ * each call fully rewrites the part it reads, so nothing needs clearing, but
+ * calls that overlap on the GPU (different streams, or different host
+ * threads on one device) race on it and must be ordered by the caller.
+ * Arguments, results and other errors are those of fa_bwd.
+ */
+#define FA_BWD_NOALLOC_MAX_ROWS (1LL << 21)
+FA_API fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v,
+                                const void *o, const void *dout,
+                                const float *lse, void *dq, void *dk, void *dv,
+                                int B, int H, int N, int d, int causal,
+                                float scale, fa_dtype dtype,
+                                fa_stream_t stream);
+
 /* A static, human-readable description of a status code. */
 FA_API const char *fa_status_string(fa_status status);
 
