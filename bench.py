@@ -54,7 +54,7 @@ DEFAULT_WORKLOAD = W.N8192.name
 # workload; reported only while the sources are unchanged (see
 # profiles/fa_fwd_kernel_b8h32n8192d64_bf16_launches.md).
 MEASURED_TRAFFIC = {
-    ("823718fbe4747852", "b8h32n8192d64_bf16"): 806.84e6 + 253.63e6,
+    ("59212b25bf6f94f3", "b8h32n8192d64_bf16"): 805.80e6 + 252.56e6,
 }
 CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw",
                 "clocks_event_reasons.active",
@@ -287,6 +287,59 @@ def run_standard(args, w, world, rank, local):
                        "method": "materialised S (dtype), fp32 softmax, torch/cuBLAS"}}
 
 
+def run_bwd(args, w, world, rank, local):
+    """The backward (fa_bwd: row sums, dQ kernel, dK/dV kernel) per step, on
+    the forward's own O and LSE.  Counted FLOPs: 2.5x the forward's
+    (10*B*H*N^2*d, half when causal), the usual convention for the five
+    products of the backward; the kernels execute seven (S and dP are
+    computed in both the dQ and the dK/dV kernel)."""
+    import exact_attention_39_gb300 as fa
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q, k, v = (t.to(dev) for t in W.make_inputs(w.with_(seed=w.seed + rank)))
+    g = W.make_upstream_grad(w).to(dev)
+    o, lse = fa.fwd(q, k, v, causal=w.causal, scale=w.scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.bwd_workspace_bytes(w.B, w.H, w.N), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        fa.bwd(q, k, v, o, lse, g, causal=w.causal, scale=w.scale, dq=dq, dk=dk,
+               dv=dv, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    with ClockSampler(local) as clocks:
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        stream.synchronize()
+    if fa.last_device_error(stream) != 0:
+        raise RuntimeError("device status set during the timed region")
+    flops = 2.5 * w.flops()
+    ms, flops_all = aggregate(t0.elapsed_time(t1), flops * args.steps, world)
+    if rank != 0:
+        return None
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    value = flops_all / (ms * 1e-3) / 1e12
+    return {"pass": "bwd", "metric": "attn bwd TFLOPS (10*B*H*N^2*d counted FLOPs, "
+            "half causal)", "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "causal": w.causal},
+            "gpu_launches": 3 * args.steps,
+            "pct_of_peak": 100.0 * value / peak,
+            "clocks": clocks.summary()}
+
+
 def run_gpu(args, w, world, rank, local):
     import exact_attention_39_gb300 as fa
 
@@ -412,6 +465,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference", "standard"], default="gb300")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="time the forward (default, the headline) or fa_bwd")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -436,6 +491,8 @@ def main(argv=None):
             line = run_reference(args, w, world, rank)
         elif args.impl == "standard":
             line = run_standard(args, w, world, rank, local)
+        elif args.pass_ == "bwd":
+            line = run_bwd(args, w, world, rank, local)
         else:
             line = run_gpu(args, w, world, rank, local)
         if line is not None:
