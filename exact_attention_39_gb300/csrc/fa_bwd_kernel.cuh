@@ -18,8 +18,10 @@
 //   fa_bwd_dkdv_kernel  one CTA per 128 keys, looping over query blocks:
 //                       S^T = K Q^T and dP^T = V dO^T (keys on TMEM lanes),
 //                       P^T and dS^T to TMEM, dV += P^T dO, dK += dS^T Q
-// Both main kernels: warps 0-3 element-wise (thread = TMEM lane), warp 4 TMA
-// producer, warp 5 TMEM allocator and MMA issuer.
+// Both main kernels: warps 0-7 element-wise in two warpgroups (thread = TMEM
+// lane; warpgroup h takes columns 64h .. 64h+63 of each 128-column block and
+// half of the output columns), warp 8 TMA producer, warp 9 TMEM allocator
+// and MMA issuer.  No row reduction crosses the halves.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -28,9 +30,11 @@
 
 namespace fa {
 
-constexpr int kBwdThreads = 192;
-constexpr int kBwdLoadWarp = 4;
-constexpr int kBwdMmaWarp = 5;
+constexpr int kBwdThreads = 320;
+constexpr int kBwdLoadWarp = 8;
+constexpr int kBwdMmaWarp = 9;
+constexpr int kBwdEwThreads = 256;       // element-wise threads
+constexpr int kBwdHalf = 64;             // columns per element-wise thread
 
 struct BwdParams {
   const void *o, *dout;      // [BH, Nq, D]
@@ -201,8 +205,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::mbar_init(bar(L::bKVEmpty + s), 1);
     }
     ptx::mbar_init(bar(L::bSFull), 1);
-    ptx::mbar_init(bar(L::bSFree), kBM);
-    ptx::mbar_init(bar(L::bDSFull), kBM);
+    ptx::mbar_init(bar(L::bSFree), kBwdEwThreads);
+    ptx::mbar_init(bar(L::bDSFull), kBwdEwThreads);
     ptx::mbar_init(bar(L::bDQDone), 1);
     ptx::mbar_init(bar(L::bDQDone + 1), 1);
     ptx::mbar_init(bar(L::bDrain), 1);
@@ -319,10 +323,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ================================================= element-wise warps
-    const int r = threadIdx.x;                      // row within the tile
+    const int h = warp >> 2;                        // column half
+    const int r = (warp & 3) * 32 + (threadIdx.x & 31);   // row = TMEM lane
     const int row = q0 + r;
     const bool valid = row < p.Nq;
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const size_t grow = (size_t)bh * (size_t)p.Nq + (size_t)row;
     float lse_l2 = 0.f, dsum = 0.f;
     if (valid) {
@@ -336,20 +341,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
       const int b = j & 1;
-      if (!wait_phase(bar(L::bSFull), j & 1, abort_flag, p)) { ok = false; break; }
+      if (!wait_warp(bar(L::bSFull), j & 1, abort_flag, p)) { ok = false; break; }
       ptx::tc_fence_after();
       if (j >= 2) {
         // dQ += dS_b K of two blocks back has finished reading dS_b
-        if (!wait_phase(bar(L::bDQDone + b), ((j - 2) >> 1) & 1, abort_flag, p)) { ok = false; break; }
+        if (!wait_warp(bar(L::bDQDone + b), ((j - 2) >> 1) & 1, abort_flag, p)) { ok = false; break; }
         ptx::tc_fence_after();
       }
-      const int lim = key_lim - j * kBN;
-      uint32_t pk[kBN / 2];
+      const int lim = key_lim - j * kBN - h * kBwdHalf;   // this half's columns >= lim: masked
+      uint32_t pk[kBwdHalf / 2];
 #pragma unroll
-      for (int cc = 0; cc < kBN; cc += 32) {
+      for (int cc = 0; cc < kBwdHalf; cc += 32) {
         uint32_t s[32], dp[32];
-        ptx::tmem_ld32(tmem + lane_off + L::tS + cc, s);
-        ptx::tmem_ld32(tmem + lane_off + L::tdP + cc, dp);
+        ptx::tmem_ld32(tmem + lane_off + L::tS + h * kBwdHalf + cc, s);
+        ptx::tmem_ld32(tmem + lane_off + L::tdP + h * kBwdHalf + cc, dp);
         ptx::tmem_wait_ld();
         ptx::reg_fence32(s);
         ptx::reg_fence32(dp);
@@ -366,25 +371,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(L::bSFree));
-#pragma unroll
-      for (int cc = 0; cc < kBN / 2; cc += 32)
-        ptx::tmem_st32(tmem + lane_off + L::tdS(b) + cc,
-                       *reinterpret_cast<uint32_t(*)[32]>(&pk[cc]));
+      ptx::tmem_st32(tmem + lane_off + L::tdS(b) + h * (kBwdHalf / 2),
+                     *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(L::bDSFull));
     }
-    // ---- epilogue: dQ = scale * (dS K)
+    // ---- epilogue: dQ = scale * (dS K), this half's columns
     if (ok && nb > 0)
-      ok = wait_phase(bar(L::bDQDone + ((nb - 1) & 1)), ((nb - 1) >> 1) & 1, abort_flag, p);
+      ok = wait_warp(bar(L::bDQDone + ((nb - 1) & 1)), ((nb - 1) >> 1) & 1, abort_flag, p);
     if (ok) {
       ptx::tc_fence_after();
-      uint16_t *out = reinterpret_cast<uint16_t *>(p.dq) + grow * D;
+      uint16_t *out = reinterpret_cast<uint16_t *>(p.dq) + grow * D + h * (D / 2);
 #pragma unroll
-      for (int cc = 0; cc < D; cc += 32) {
+      for (int cc = 0; cc < D / 2; cc += 32) {
         uint32_t g[32];
         if (nb > 0) {
-          ptx::tmem_ld32(tmem + lane_off + L::tdQ + cc, g);
+          ptx::tmem_ld32(tmem + lane_off + L::tdQ + h * (D / 2) + cc, g);
           ptx::tmem_wait_ld();
           ptx::reg_fence32(g);
         } else {
@@ -456,8 +459,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::mbar_init(bar(L::bQEmpty + s), 1);
     }
     ptx::mbar_init(bar(L::bSFull), 1);
-    ptx::mbar_init(bar(L::bSFree), kBM);
-    ptx::mbar_init(bar(L::bPFull), kBM);
+    ptx::mbar_init(bar(L::bSFree), kBwdEwThreads);
+    ptx::mbar_init(bar(L::bPFull), kBwdEwThreads);
     ptx::mbar_init(bar(L::bPDone), 1);
     ptx::mbar_init(bar(L::bDrain), 1);
     *abort_flag = 0;
@@ -597,75 +600,83 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ================================================= element-wise warps
-    const int r = threadIdx.x;                      // key within the block
+    const int h = warp >> 2;                        // query-column half
+    const int r = (warp & 3) * 32 + (threadIdx.x & 31);   // key = TMEM lane
     const int key = k0 + r;
-    const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float c = p.c;
     const int shift = p.Nk - p.Nq;                  // causal: key <= row + shift
     bool ok = true;
     for (int n = 0; n < nqb; ++n) {
       const int i = i_begin + n;
       const int st = n % L::kStages;
-      if (!wait_phase(bar(L::bSFull), n & 1, abort_flag, p) ||
-          !wait_phase(bar(L::bQFull + st), (n / L::kStages) & 1, abort_flag, p)) {
+      if (!wait_warp(bar(L::bSFull), n & 1, abort_flag, p) ||
+          !wait_warp(bar(L::bQFull + st), (n / L::kStages) & 1, abort_flag, p)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
-      const float *lse_s = reinterpret_cast<const float *>(sm.smem + L::stage(st) + 2 * L::kTile);
+      const float *lse_s = reinterpret_cast<const float *>(sm.smem + L::stage(st) + 2 * L::kTile) +
+                           h * kBwdHalf;
       const float *d_s = lse_s + kBM;
-      // columns (query rows) before `first` do not see this key
-      const int first = p.causal ? key - shift - i * kBM : 0;
-      uint32_t pkp[kBM / 2], pkd[kBM / 2];
+      // columns (query rows) of this half before `first` do not see the key
+      const int first = p.causal ? key - shift - i * kBM - h * kBwdHalf : 0;
+      uint32_t pkp[kBwdHalf / 2], pkd[kBwdHalf / 2];
 #pragma unroll
-      for (int cc = 0; cc < kBM; cc += 32) {
+      for (int cc = 0; cc < kBwdHalf; cc += 32) {
         uint32_t s[32], dp[32];
-        ptx::tmem_ld32(tmem + lane_off + L::tS + cc, s);
-        ptx::tmem_ld32(tmem + lane_off + L::tdP + cc, dp);
+        ptx::tmem_ld32(tmem + lane_off + L::tS + h * kBwdHalf + cc, s);
+        ptx::tmem_ld32(tmem + lane_off + L::tdP + h * kBwdHalf + cc, dp);
         ptx::tmem_wait_ld();
         ptx::reg_fence32(s);
         ptx::reg_fence32(dp);
 #pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          float pr0 = ptx::ex2_approx(fmaf(__uint_as_float(s[t]), c, -lse_s[cc + t]));
-          float pr1 = ptx::ex2_approx(fmaf(__uint_as_float(s[t + 1]), c, -lse_s[cc + t + 1]));
-          if (cc + t < first) pr0 = 0.f;
-          if (cc + t + 1 < first) pr1 = 0.f;
-          const float ds0 = pr0 * (__uint_as_float(dp[t]) - d_s[cc + t]);
-          const float ds1 = pr1 * (__uint_as_float(dp[t + 1]) - d_s[cc + t + 1]);
-          pkp[(cc + t) / 2] = pack2<T>(pr0, pr1);
-          pkd[(cc + t) / 2] = pack2<T>(ds0, ds1);
+        for (int t = 0; t < 32; t += 4) {
+          const float4 l4 = *reinterpret_cast<const float4 *>(lse_s + cc + t);
+          const float4 d4 = *reinterpret_cast<const float4 *>(d_s + cc + t);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pr[4], ds[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            pr[u] = ptx::ex2_approx(fmaf(__uint_as_float(s[t + u]), c, -lv[u]));
+            if (cc + t + u < first) pr[u] = 0.f;
+            ds[u] = pr[u] * (__uint_as_float(dp[t + u]) - dv4[u]);
+          }
+          pkp[(cc + t) / 2] = pack2<T>(pr[0], pr[1]);
+          pkp[(cc + t) / 2 + 1] = pack2<T>(pr[2], pr[3]);
+          pkd[(cc + t) / 2] = pack2<T>(ds[0], ds[1]);
+          pkd[(cc + t) / 2 + 1] = pack2<T>(ds[2], ds[3]);
         }
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(L::bSFree));
       if (n > 0) {
         // the gradient MMAs of the previous block have read P^T and dS^T
-        if (!wait_phase(bar(L::bPDone), (n - 1) & 1, abort_flag, p)) { ok = false; break; }
+        if (!wait_warp(bar(L::bPDone), (n - 1) & 1, abort_flag, p)) { ok = false; break; }
         ptx::tc_fence_after();
       }
-#pragma unroll
-      for (int cc = 0; cc < kBM / 2; cc += 32) {
-        ptx::tmem_st32(tmem + lane_off + L::tP + cc, *reinterpret_cast<uint32_t(*)[32]>(&pkp[cc]));
-        ptx::tmem_st32(tmem + lane_off + L::tdS + cc, *reinterpret_cast<uint32_t(*)[32]>(&pkd[cc]));
-      }
+      ptx::tmem_st32(tmem + lane_off + L::tP + h * (kBwdHalf / 2),
+                     *reinterpret_cast<uint32_t(*)[32]>(&pkp[0]));
+      ptx::tmem_st32(tmem + lane_off + L::tdS + h * (kBwdHalf / 2),
+                     *reinterpret_cast<uint32_t(*)[32]>(&pkd[0]));
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(L::bPFull));
     }
-    // ---- epilogue: dV and dK = scale * (dS^T Q)
-    if (ok && nqb > 0) ok = wait_phase(bar(L::bPDone), (nqb - 1) & 1, abort_flag, p);
+    // ---- epilogue: dV and dK = scale * (dS^T Q), this half's columns
+    if (ok && nqb > 0) ok = wait_warp(bar(L::bPDone), (nqb - 1) & 1, abort_flag, p);
     if (ok) {
       ptx::tc_fence_after();
       const bool valid = key < p.Nk;
       const size_t gk = (size_t)bh * (size_t)p.Nk + (size_t)key;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        uint16_t *out = reinterpret_cast<uint16_t *>(which == 0 ? p.dv : p.dk) + gk * D;
-        const uint32_t tcol = which == 0 ? L::tdV : L::tdK;
+        uint16_t *out = reinterpret_cast<uint16_t *>(which == 0 ? p.dv : p.dk) + gk * D +
+                        h * (D / 2);
+        const uint32_t tcol = (which == 0 ? L::tdV : L::tdK) + h * (D / 2);
         const float mul = which == 0 ? 1.f : p.scale;
 #pragma unroll
-        for (int cc = 0; cc < D; cc += 32) {
+        for (int cc = 0; cc < D / 2; cc += 32) {
           uint32_t g[32];
           if (nqb > 0) {
             ptx::tmem_ld32(tmem + lane_off + tcol + cc, g);
