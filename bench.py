@@ -54,7 +54,7 @@ DEFAULT_WORKLOAD = W.N8192.name
 # workload; reported only while the sources are unchanged (see
 # profiles/fa_fwd_kernel_b8h32n8192d64_bf16_launches.md).
 MEASURED_TRAFFIC = {
-    ("59212b25bf6f94f3", "b8h32n8192d64_bf16"): 805.80e6 + 252.56e6,
+    ("fa7fd3205794918a", "b8h32n8192d64_bf16"): 805.80e6 + 252.56e6,
 }
 CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw",
                 "clocks_event_reasons.active",
@@ -66,10 +66,12 @@ CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw",
 
 # ---------------------------------------------------------------- helpers
 def kernel_source_hash():
+    """Hash of the forward kernel's device sources (the traffic figures
+    below were captured with exactly these)."""
     import hashlib
     csrc = os.path.join(ROOT, "exact_attention_39_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("fa_api.cu", "fa_fwd_kernel.cuh", "ptx.cuh"):
+    for f in ("fa_fwd_kernel.cuh", "ptx.cuh"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

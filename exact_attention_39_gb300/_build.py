@@ -9,7 +9,7 @@ LIB_NAME = "libfa_sm103.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 SOURCES = ["fa_api.cu"]
 DEPS = ["fa_fwd_kernel.cuh", "fa_bwd_kernel.cuh", "ptx.cuh"]
-HEADERS = ["fa.h"]
+HEADERS = ["fa.h", "fa_selftest.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

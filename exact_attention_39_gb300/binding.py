@@ -28,7 +28,7 @@ FA_BF16 = 1
 
 EXPORTED = ("fa_fwd", "fa_fwd_qk", "fa_fwd_fp8", "fa_bwd", "fa_bwd_workspace_bytes",
             "fa_bwd_noalloc", "fa_status_string", "fa_last_device_error",
-            "fa_version")
+            "fa_version", "fa_selftest_wait_timeout")
 FA_BWD_NOALLOC_MAX_ROWS = 1 << 21
 
 _lib = None
@@ -67,6 +67,8 @@ def load_library(path=None):
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i,
                                    i, f, i, vp]
     lib.fa_bwd_noalloc.restype = i
+    lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
+    lib.fa_selftest_wait_timeout.restype = i
     lib.fa_status_string.argtypes = [i]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_device_error.argtypes = [vp]
@@ -298,3 +300,9 @@ def last_device_error(stream=None):
 
 def version():
     return load_library().fa_version()
+
+
+def selftest_wait_timeout(timeout_ns, stream=None):
+    """Enqueue the bounded-wait self-test kernel; returns the launch status."""
+    return load_library().fa_selftest_wait_timeout(int(timeout_ns),
+                                                   _stream_handle(stream))

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_selftest.h"
 #include "fa_bwd_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 
@@ -135,6 +136,26 @@ fa_status run(const void *q, const void *k, const void *v, FwdParams p,
 }
 
 bool aligned(const void *p, uintptr_t a);
+
+struct WaitTestParams {
+  unsigned long long timeout_ns;
+  unsigned *status;
+};
+
+// One warp waits, with the kernels' bounded wait, on a phase of an mbarrier
+// that expects one arrival nobody makes.
+__global__ void fa_selftest_wait_kernel(const WaitTestParams p) {
+  __shared__ uint64_t mbar;
+  __shared__ int abort_flag;
+  const uint32_t b = ptx::smem_u32(&mbar);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(b, 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncwarp();
+  wait_warp(b, 0, &abort_flag, p);
+}
 
 // Encodes the four maps and launches the three backward kernels.
 template <int D, int T>
@@ -363,6 +384,21 @@ fa_status fa_last_device_error(fa_stream_t stream) {
 }
 
 int fa_version(void) { return 100; }
+
+fa_status fa_selftest_wait_timeout(unsigned long long timeout_ns,
+                                   fa_stream_t stream) {
+  using namespace fa;
+  if (timeout_ns < 1000ull || timeout_ns > 1000000000ull) return FA_ERR_SHAPE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  const fa_status st = ensure_ready(dev);
+  if (st != FA_OK) return st;
+  WaitTestParams p;
+  p.timeout_ns = timeout_ns;
+  p.status = g_status_ptr[dev];
+  fa_selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
 
 }  // extern "C"
 
