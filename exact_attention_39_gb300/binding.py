@@ -26,7 +26,7 @@ FA_ERR_WORKSPACE = 9
 FA_FP16 = 0
 FA_BF16 = 1
 
-EXPORTED = ("fa_fwd", "fa_fwd_qk", "fa_fwd_fp8", "fa_bwd", "fa_bwd_workspace_bytes",
+EXPORTED = ("fa_fwd", "fa_fwd_qk", "fa_fwd_fp8", "fa_fwd_host", "fa_bwd", "fa_bwd_workspace_bytes",
             "fa_bwd_noalloc", "fa_status_string", "fa_last_device_error",
             "fa_version", "fa_selftest_wait_timeout")
 FA_BWD_NOALLOC_MAX_ROWS = 1 << 21
@@ -58,6 +58,8 @@ def load_library(path=None):
     lib.fa_fwd_qk.restype = i
     lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, f, f, f, vp]
     lib.fa_fwd_fp8.restype = i
+    lib.fa_fwd_host.argtypes = [vp] * 10 + [i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_host.restype = i
     sz = ctypes.c_size_t
     lib.fa_bwd_workspace_bytes.argtypes = [i, i, i]
     lib.fa_bwd_workspace_bytes.restype = sz
@@ -274,21 +276,45 @@ def bwd(q, k, v, o, lse, dout, causal=False, scale=None, dq=None, dk=None,
     return dq, dk, dv
 
 
+def fa_fwd_host_raw(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d,
+                    B, H, N, d, causal, scale, dtype_code, stream_handle):
+    """The C call with plain integers; returns the status code."""
+    return load_library().fa_fwd_host(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d,
+                                      o_d, lse_d, int(B), int(H), int(N), int(d),
+                                      int(bool(causal)), float(scale),
+                                      int(dtype_code), stream_handle)
+
+
 def fwd_host(q_h, k_h, v_h, q_d, k_d, v_d, o_d, lse_d, o_h, lse_h,
              causal=False, scale=None, stream=None):
-    """End-to-end call from host memory: copy q, k, v (pinned host tensors)
-    into the device buffers, run ``fa_fwd``, copy O and LSE back into the
-    pinned host tensors ``o_h``/``lse_h``.  All copies and the kernel are
-    enqueued on one stream; the call returns after synchronising it."""
+    """End-to-end call from host memory through ``fa_fwd_host``: q, k, v
+    (pinned host tensors) go up through the device staging buffers, O and LSE
+    come back into the pinned host tensors ``o_h``/``lse_h``; the library
+    overlaps the copies with the kernel chunk by chunk.  Returns after
+    synchronising ``stream``."""
+    for t in (q_h, k_h, v_h, o_h, lse_h):
+        if t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError("host tensors must be contiguous CPU tensors")
+    for t in (q_d, k_d, v_d, o_d, lse_d):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("staging tensors must be contiguous CUDA tensors")
+    if q_h.dim() != 4 or k_h.shape != q_h.shape or v_h.shape != q_h.shape:
+        raise ValueError("q, k, v must share one [B, H, N, d] shape")
+    for a, b in ((q_h, q_d), (k_h, k_d), (v_h, v_d), (o_h, o_d), (lse_h, lse_d)):
+        if a.shape != b.shape or a.dtype != b.dtype:
+            raise ValueError("host and staging tensors disagree in shape or dtype")
+    if o_h.shape != q_h.shape or o_h.dtype != q_h.dtype:
+        raise ValueError("o must match q")
+    B, H, N, d = q_h.shape
+    if lse_h.shape != (B, H, N) or lse_h.dtype != torch.float32:
+        raise ValueError("lse must be float32 [B, H, N]")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
     stream = stream or torch.cuda.current_stream()
-    with torch.cuda.stream(stream):
-        q_d.copy_(q_h, non_blocking=True)
-        k_d.copy_(k_h, non_blocking=True)
-        v_d.copy_(v_h, non_blocking=True)
-        fwd(q_d, k_d, v_d, causal=causal, scale=scale, out=o_d, lse=lse_d,
-            stream=stream)
-        o_h.copy_(o_d, non_blocking=True)
-        lse_h.copy_(lse_d, non_blocking=True)
+    _check(fa_fwd_host_raw(q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(),
+                           o_h.data_ptr(), lse_h.data_ptr(), q_d.data_ptr(),
+                           k_d.data_ptr(), v_d.data_ptr(), o_d.data_ptr(),
+                           lse_d.data_ptr(), B, H, N, d, causal, scale,
+                           _dtype_code(q_h), _stream_handle(stream)))
     stream.synchronize()
     return o_h, lse_h
 

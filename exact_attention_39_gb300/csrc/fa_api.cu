@@ -137,6 +137,22 @@ fa_status run(const void *q, const void *k, const void *v, FwdParams p,
 
 bool aligned(const void *p, uintptr_t a);
 
+// Streams of the host-buffer pipeline (upload, compute, download), created
+// once per device.
+constexpr int kPipeStreams = 3;
+cudaStream_t g_pipe[kMaxDevices][kPipeStreams] = {};
+
+fa_status pipe_streams(int dev, cudaStream_t **out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_pipe[dev][0]) {
+    for (int t = 0; t < kPipeStreams; ++t)
+      if (cudaStreamCreateWithFlags(&g_pipe[dev][t], cudaStreamNonBlocking) != cudaSuccess)
+        return FA_ERR_CUDA;
+  }
+  *out = g_pipe[dev];
+  return FA_OK;
+}
+
 struct WaitTestParams {
   unsigned long long timeout_ns;
   unsigned *status;
@@ -283,6 +299,88 @@ fa_status fa_fwd_fp8(const void *q, const void *k, const void *v, void *o,
   p.status = g_status_ptr[dev];
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return d == 64 ? run<64, kE4M3>(q, k, v, p, bh, s) : run<128, kE4M3>(q, k, v, p, bh, s);
+}
+
+fa_status fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
+                      void *o_h, float *lse_h, void *q_d, void *k_d, void *v_d,
+                      void *o_d, float *lse_d, int B, int H, int N, int d,
+                      int causal, float scale, fa_dtype dtype,
+                      fa_stream_t stream) {
+  using namespace fa;
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+  if (B == 0 || H == 0 || N == 0) return FA_OK;
+  if (!q_h || !k_h || !v_h || !o_h || !lse_h || !q_d || !k_d || !v_d || !o_d || !lse_d)
+    return FA_ERR_NULL;
+  if (!aligned(q_d, 16) || !aligned(k_d, 16) || !aligned(v_d, 16) || !aligned(o_d, 16) ||
+      !aligned(lse_d, 4))
+    return FA_ERR_ALIGN;
+  const long long bh = (long long)B * (long long)H;
+  if (bh > (1ll << 31) - 1) return FA_ERR_SHAPE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  fa_status st = ensure_ready(dev);
+  if (st != FA_OK) return st;
+  cudaStream_t *ps = nullptr;
+  if ((st = pipe_streams(dev, &ps)) != FA_OK) return st;
+  cudaStream_t up = ps[0], comp = ps[1], down = ps[2];
+  cudaStream_t caller = reinterpret_cast<cudaStream_t>(stream);
+
+  // chunks of whole (batch, head) problems: up to 8, each at least one
+  const long long chunks = bh < 8 ? bh : 8;
+  const size_t row_bytes = (size_t)d * 2u;
+  const size_t head_bytes = (size_t)N * row_bytes, head_lse = (size_t)N * sizeof(float);
+  cudaEvent_t start, ev_in[8], ev_out[8], done;
+  if (cudaEventCreateWithFlags(&start, cudaEventDisableTiming) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaEventCreateWithFlags(&done, cudaEventDisableTiming) != cudaSuccess) return FA_ERR_CUDA;
+  for (int c = 0; c < chunks; ++c)
+    if (cudaEventCreateWithFlags(&ev_in[c], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ev_out[c], cudaEventDisableTiming) != cudaSuccess)
+      return FA_ERR_CUDA;
+  bool ok = cudaEventRecord(start, caller) == cudaSuccess &&
+            cudaStreamWaitEvent(up, start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(comp, start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(down, start, 0) == cudaSuccess;
+  for (long long c = 0; ok && c < chunks; ++c) {
+    const long long h0 = bh * c / chunks, h1 = bh * (c + 1) / chunks, nh = h1 - h0;
+    const size_t off = (size_t)h0 * head_bytes, bytes = (size_t)nh * head_bytes;
+    const size_t loff = (size_t)h0 * head_lse, lbytes = (size_t)nh * head_lse;
+    char *qd = static_cast<char *>(q_d) + off, *kd = static_cast<char *>(k_d) + off;
+    char *vd = static_cast<char *>(v_d) + off, *od = static_cast<char *>(o_d) + off;
+    float *ld = reinterpret_cast<float *>(reinterpret_cast<char *>(lse_d) + loff);
+    ok = cudaMemcpyAsync(qd, static_cast<const char *>(q_h) + off, bytes,
+                         cudaMemcpyHostToDevice, up) == cudaSuccess &&
+         cudaMemcpyAsync(kd, static_cast<const char *>(k_h) + off, bytes,
+                         cudaMemcpyHostToDevice, up) == cudaSuccess &&
+         cudaMemcpyAsync(vd, static_cast<const char *>(v_h) + off, bytes,
+                         cudaMemcpyHostToDevice, up) == cudaSuccess &&
+         cudaEventRecord(ev_in[c], up) == cudaSuccess &&
+         cudaStreamWaitEvent(comp, ev_in[c], 0) == cudaSuccess;
+    if (!ok) break;
+    st = fa_fwd_qk(qd, kd, vd, od, ld, 1, (int)nh, N, N, d, causal, scale, dtype,
+                   reinterpret_cast<fa_stream_t>(comp));
+    if (st != FA_OK) { ok = false; break; }
+    ok = cudaEventRecord(ev_out[c], comp) == cudaSuccess &&
+         cudaStreamWaitEvent(down, ev_out[c], 0) == cudaSuccess &&
+         cudaMemcpyAsync(static_cast<char *>(o_h) + off, od, bytes,
+                         cudaMemcpyDeviceToHost, down) == cudaSuccess &&
+         cudaMemcpyAsync(reinterpret_cast<char *>(lse_h) + loff, ld, lbytes,
+                         cudaMemcpyDeviceToHost, down) == cudaSuccess;
+  }
+  if (ok)
+    ok = cudaEventRecord(done, down) == cudaSuccess &&
+         cudaStreamWaitEvent(caller, done, 0) == cudaSuccess;
+  // events are released once the work they mark has completed
+  cudaEventDestroy(start);
+  cudaEventDestroy(done);
+  for (int c = 0; c < chunks; ++c) {
+    cudaEventDestroy(ev_in[c]);
+    cudaEventDestroy(ev_out[c]);
+  }
+  if (!ok) return st != FA_OK ? st : FA_ERR_CUDA;
+  return FA_OK;
 }
 
 fa_status fa_fwd(const void *q, const void *k, const void *v, void *o,

@@ -137,6 +137,28 @@ FA_API fa_status fa_fwd_fp8(const void *q, const void *k, const void *v,
                             fa_stream_t stream);
 
 /*
+ * fa_fwd_host -- fa_fwd from and to host memory, with the copies overlapped.
+ *
+ *   q_h, k_h, v_h    : host [B, H, N, d] inputs (page-locked memory lets the
+ *                      copies run asynchronously and overlap).
+ *   o_h, lse_h       : host outputs, [B, H, N, d] dtype and [B, H, N] fp32.
+ *   q_d, k_d, v_d, o_d, lse_d : caller-owned device staging buffers of the
+ *                      same shapes (alignment as fa_fwd).
+ * The B*H problems are split into chunks; the upload of one chunk, the
+ * forward kernel of the previous one and the download of the one before
+ * run concurrently on the library's own streams.  All of it is ordered
+ * after the work already enqueued on `stream`, and `stream` waits for the
+ * last download, so synchronising `stream` makes o_h and lse_h valid.
+ * Errors as fa_fwd (checked before anything is enqueued), plus FA_ERR_NULL
+ * for a missing host or staging buffer.
+ */
+FA_API fa_status fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
+                             void *o_h, float *lse_h, void *q_d, void *k_d,
+                             void *v_d, void *o_d, float *lse_d, int B, int H,
+                             int N, int d, int causal, float scale,
+                             fa_dtype dtype, fa_stream_t stream);
+
+/*
  * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs for
  * B*H*N query rows (one fp32 per row, rounded up to 256 bytes).
  */

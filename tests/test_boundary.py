@@ -86,6 +86,24 @@ def test_host_side_checks_qk(kw, code):
     assert call_qk(**kw) == code
 
 
+def call_host(q=P, k=P, v=P, o=P, lse=P, qd=P, kd=P, vd=P, od=P, ld=P, B=1, H=1,
+              N=128, d=64, causal=0, scale=0.125, dtype=b.FA_BF16):
+    return b.fa_fwd_host_raw(q, k, v, o, lse, qd, kd, vd, od, ld, B, H, N, d,
+                             causal, scale, dtype, ctypes.c_void_p(0))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=NULL), b.FA_ERR_NULL), (dict(o=NULL), b.FA_ERR_NULL),
+    (dict(lse=NULL), b.FA_ERR_NULL), (dict(vd=NULL), b.FA_ERR_NULL),
+    (dict(ld=NULL), b.FA_ERR_NULL), (dict(B=-1), b.FA_ERR_SHAPE),
+    (dict(d=96), b.FA_ERR_HEADDIM), (dict(dtype=2), b.FA_ERR_DTYPE),
+    (dict(scale=0.0), b.FA_ERR_SCALE), (dict(kd=P + 8), b.FA_ERR_ALIGN),
+    (dict(ld=P + 2), b.FA_ERR_ALIGN),
+])
+def test_host_side_checks_host_buffers(kw, code):
+    assert call_host(**kw) == code
+
+
 def test_empty_problems_launch_nothing():
     # B, H or N equal to zero is an empty problem: FA_OK, nothing enqueued,
     # pointers never looked at.
@@ -93,12 +111,15 @@ def test_empty_problems_launch_nothing():
         assert call(q=NULL, k=NULL, v=NULL, o=NULL, lse=NULL, **kw) == b.FA_OK
     for kw in (dict(B=0), dict(H=0), dict(Nq=0)):
         assert call_qk(q=NULL, k=NULL, v=NULL, o=NULL, lse=NULL, **kw) == b.FA_OK
+    for kw in (dict(B=0), dict(H=0), dict(N=0)):
+        assert call_host(q=NULL, qd=NULL, o=NULL, ld=NULL, **kw) == b.FA_OK
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="needs a machine without a GPU")
 def test_no_cpu_fallback_without_gpu():
     # Valid arguments but no CUDA device: the call must fail, not compute.
     assert call() == b.FA_ERR_CUDA
+    assert call_host() == b.FA_ERR_CUDA
     q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.fwd(q, q, q)

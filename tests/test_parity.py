@@ -229,6 +229,29 @@ def test_host_buffers_end_to_end():
     check(w, oh, lh, q, k, v)
 
 
+@pytest.mark.parametrize("B,H,N,causal,dtype", [
+    (1, 1, 200, False, "fp16"), (1, 5, 384, True, "bf16"),
+    (3, 7, 300, True, "bf16"), (2, 16, 1024, False, "bf16")])
+def test_host_buffers_match_device_call(B, H, N, causal, dtype):
+    # The chunked host-buffer pipeline runs the same kernel per (batch, head)
+    # problem, so its outputs equal the device-buffer call bit for bit, for
+    # head counts that do and do not divide into the chunks.
+    w = W.Workload("host", B, H, N, 64, dtype, causal, seed=21)
+    q, k, v = W.make_inputs(w)
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    dev = [torch.empty_like(t, device="cuda") for t in (q, k, v)]
+    od = torch.empty_like(dev[0])
+    ld = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    oh = torch.empty_like(q).pin_memory()
+    lh = torch.empty(B, H, N, dtype=torch.float32).pin_memory()
+    fa.fwd_host(qh, kh, vh, *dev, od, ld, oh, lh, causal=causal, scale=w.scale)
+    o_ref, l_ref = fa.fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal,
+                          scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, l_ref.cpu())
+    assert fa.last_device_error() == 0
+
+
 def test_outputs_do_not_touch_neighbours():
     # O and LSE are written only inside their [B, H, N, d] / [B, H, N] spans.
     w = W.Workload("guard", 1, 2, 300, 64, "bf16", True, seed=8)
