@@ -42,6 +42,8 @@ from exact_attention_39_gb300 import workloads as W  # noqa: E402
 
 METRIC = "attn fwd TFLOPS & % of GB300 BF16 tensor peak (B8 H32 d64, N=512–8192)"
 UNIT = "TFLOPS"
+# NVIDIA's dense (no 2:4 sparsity) bf16 tensor figure for one GB300 GPU.
+DATASHEET_TFLOPS = 2250.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
                   "bf16_tflops_sustained": 1700.0}
 WORKLOADS = {w.name: w for w in
@@ -188,9 +190,12 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def time_oracle(w, budget_s, max_heads):
+def time_oracle(w, budget_s, max_heads, rows_1t=256):
     """Time the fp64 oracle on whole heads of ``w`` until ``budget_s`` of
-    work is done.  Returns (seconds, flops, heads, threads)."""
+    work is done, on every host core; then on one core, ``rows_1t`` evenly
+    spaced query rows of one head.  Returns (seconds, flops, heads, threads,
+    one-core flop/s)."""
+    import numpy as np
     import oracle
     q, k, v = W.make_inputs(w.with_(B=1, H=max_heads))
     nt = oracle.default_threads()
@@ -204,7 +209,14 @@ def time_oracle(w, budget_s, max_heads):
         heads += 1
         if secs >= budget_s:
             break
-    return secs, flops, heads, nt
+    qh, kh, vh = (t[0, 0].double().numpy() for t in (q, k, v))
+    rows = min(w.N, rows_1t)
+    sel = np.arange(rows, dtype=np.int64) * (w.N // rows)
+    t0 = time.perf_counter()
+    oracle.attention_fwd(qh, kh, vh, w.scale, w.causal, rows=sel, nthreads=1)
+    one = time.perf_counter() - t0
+    row_flops = 4.0 * w.n_keys * w.d / (2.0 if w.causal else 1.0)
+    return secs, flops, heads, nt, row_flops * rows / one
 
 
 # ---------------------------------------------------------------- arms
@@ -425,6 +437,13 @@ def run_gpu(args, w, world, rank, local):
     peak_mult = 2.0 if fp8 else 1.0
     peak *= peak_mult
     achieved = w.flops() / (kern_avg_ms * 1e-3) / 1e12
+    kern_sorted = sorted(kernel_ms)
+    kern_med = kern_sorted[len(kern_sorted) // 2]
+    props = torch.cuda.get_device_properties(dev)
+    clk = clocks.summary()
+    sm_mhz = clk.get("sm_mhz") or 0
+    # one exponential per visible score: N*Nk per head, about half when causal
+    exps = w.B * w.H * w.N * w.n_keys / (2.0 if w.causal else 1.0)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_source": ("%s bf16 burst (MEASURED_PEAKS.json)" % src
@@ -434,14 +453,21 @@ def run_gpu(args, w, world, rank, local):
                 MEASURED_TRAFFIC.get((kernel_source_hash(), w.name)),
                 "algorithmic_bytes": w.hbm_bytes(),
                 "kernel_ms": kern_avg_ms,
+                "kernel_ms_median": kern_med, "kernel_ms_min": kern_sorted[0],
+                "pct_of_datasheet": 100.0 * achieved / (DATASHEET_TFLOPS * peak_mult),
+                "exp_per_clk_per_sm": (exps / (kern_avg_ms * 1e-3)
+                                       / (sm_mhz * 1e6 * props.multi_processor_count)
+                                       if sm_mhz else None),
                 "hbm_gbs_algorithmic": w.hbm_bytes() / (kern_avg_ms * 1e-3) / 1e9}
     cpu = None
     if not args.no_cpu_baseline:
-        secs, fl, heads, nt = time_oracle(w, args.cpu_budget, args.cpu_max_heads)
+        secs, fl, heads, nt, one = time_oracle(w, args.cpu_budget, args.cpu_max_heads)
         cpu = {"value": fl / secs / 1e12, "unit": UNIT, "cores": nt,
                "kind": "oracle",
                "sample": "%d whole head(s) (all %d query rows) of %s, fp64, %.1f s"
-                         % (heads, w.N, w.name, secs)}
+                         % (heads, w.N, w.name, secs),
+               "value_1_core": one / 1e12,
+               "sample_1_core": "256 evenly spaced query rows of one head, 1 thread"}
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -456,7 +482,7 @@ def run_gpu(args, w, world, rank, local):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "clocks": clocks.summary(),
+        "clocks": clk,
     }
 
 
