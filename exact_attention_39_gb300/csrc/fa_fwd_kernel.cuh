@@ -18,14 +18,17 @@
 //   warps 10-11 idle (they complete the third warpgroup, which lets the
 //              register budget be moved to the softmax warpgroups)
 //
-// Per key block j the MMA thread issues, in this order,
-//   PV_0(j-1)... i.e.   O_0 += P_0 V_j ; S_0 = Q_0 K_{j+1}^T ;
-//                       O_1 += P_1 V_j ; S_1 = Q_1 K_{j+1}^T
-// so that while one softmax warpgroup works on its scores the tensor core
-// works for the other (ping-pong).  A commit after S_i(j+1) tracks every
-// earlier MMA of the thread, so when a softmax warpgroup sees S_i(j+1) ready
-// it also knows that O_i += P_i V_j has finished: it may then rescale O_i and
-// overwrite P_i.
+// Per key block j the MMA thread issues, for D = 64 (P has TMEM columns of
+// its own):
+//   S_0 = Q_0 K_{j+1}^T, S_1 = Q_1 K_{j+1}^T   once both warpgroups have read
+//                                               their block-j scores;
+//   O_0 += P_0 V_j,      O_1 += P_1 V_j        once both have written P(j);
+// so the next scores are computed while softmax works on the current ones.
+// For D = 128 (P over the first columns of S_i) it issues, tile by tile,
+// O_i += P_i V_j and then S_i = Q_i K_{j+1}^T: the tensor pipe runs one
+// thread's MMAs in order, so the product reads P_i before the next scores
+// overwrite it.  A commit after each O_i += P_i V_j (o_done) tells softmax
+// warpgroup i that it may rescale O_i and overwrite P_i.
 //
 // TMEM (512 columns, fp32 cells, 128 lanes):
 //   S_i  at columns i*128 .. i*128+127   (scores of tile i, one row per lane)
@@ -139,6 +142,12 @@ struct Layout {
   // the MMA for the next block's scores may overwrite S_i as soon as softmax
   // has read it.
   static constexpr bool kEarlyS = 256 + 2 * D + 2 * kPCols <= kTmemCols;
+  // With the early scores the MMA thread keeps its per-block waits to three:
+  // K and V of a stage land on one barrier, and one barrier each counts both
+  // warpgroups' "scores read" and "P written" arrivals.  (The thread shares
+  // its sub-partition with two softmax warps, so each wait it makes costs
+  // issue slots that delay every later MMA.)
+  static constexpr bool kMerged = kEarlyS;
   // TMEM columns
   __host__ __device__ static constexpr uint32_t tS(int i) { return i * 128; }
   __host__ __device__ static constexpr uint32_t tO(int i) { return 256 + i * D; }
@@ -259,14 +268,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(L::bQFull), 1);
     for (int s = 0; s < L::kStages; ++s) {
-      ptx::mbar_init(bar(L::bKFull + s), 1);
+      ptx::mbar_init(bar(L::bKFull + s), 1);   // K, or K and V when merged
       ptx::mbar_init(bar(L::bVFull + s), 1);
       ptx::mbar_init(bar(L::bKVEmpty + s), 1);
     }
     for (int i = 0; i < kNumQ; ++i) {
       ptx::mbar_init(bar(L::bSFull + i), 1);
-      ptx::mbar_init(bar(L::bSFree + i), kBM);
-      ptx::mbar_init(bar(L::bPFull + i), kBM);
+      // merged: barrier 0 of each pair counts both warpgroups
+      ptx::mbar_init(bar(L::bSFree + i), L::kMerged ? kNumQ * kBM : kBM);
+      ptx::mbar_init(bar(L::bPFull + i), L::kMerged ? kNumQ * kBM : kBM);
       ptx::mbar_init(bar(L::bODone + i), 1);
     }
     ptx::mbar_init(bar(L::bDrain), 1);
@@ -309,14 +319,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             !wait_warp(bar(L::bKVEmpty + st), (use - 1) & 1, abort_flag, p))
           break;
         if (leader) {
-          ptx::mbar_arrive_expect_tx(bar(L::bKFull + st), L::kTileBytes);
+          const uint32_t vbar = bar(L::kMerged ? L::bKFull + st : L::bVFull + st);
+          ptx::mbar_arrive_expect_tx(bar(L::bKFull + st),
+                                     L::kMerged ? 2 * L::kTileBytes : L::kTileBytes);
           for (int c = 0; c < L::kChunks; ++c)
             ptx::tma_load_3d(sbase + L::kK + st * L::kTileBytes + c * L::kChunkBytes,
                              &tmK, bar(L::bKFull + st), c * L::kChunkElems, j * kBN, bh, pol_kv);
-          ptx::mbar_arrive_expect_tx(bar(L::bVFull + st), L::kTileBytes);
+          if (!L::kMerged) ptx::mbar_arrive_expect_tx(vbar, L::kTileBytes);
           for (int c = 0; c < L::kChunks; ++c)
             ptx::tma_load_3d(sbase + L::kV + st * L::kTileBytes + c * L::kChunkBytes,
-                             &tmV, bar(L::bVFull + st), c * L::kChunkElems, j * kBN, bh, pol_kv);
+                             &tmV, vbar, c * L::kChunkElems, j * kBN, bh, pol_kv);
         }
         issued = j + 1;
       }
@@ -328,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = j % L::kStages;
         const uint32_t ph = (uint32_t)(j / L::kStages) & 1u;
         wait_drain(bar(L::bKFull + st), ph, p);
-        wait_drain(bar(L::bVFull + st), ph, p);
+        if (!L::kMerged) wait_drain(bar(L::bVFull + st), ph, p);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -386,36 +398,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         for (int i = 0; i < kNumQ; ++i) issue_s(i, 0);
       }
-      for (int j = 0; ok && j < nb; ++j) {
-        const int st = j % L::kStages;
-        const int st2 = (j + 1) % L::kStages;
-        const bool more = j + 1 < nb;
-        if (L::kEarlyS && more) {
-          // Scores of block j+1 as soon as each softmax warpgroup has its
-          // block-j scores in registers.
-          if (!wait_warp(bar(L::bKFull + st2), ((j + 1) / L::kStages) & 1, abort_flag, p)) break;
-          for (int i = 0; i < kNumQ && ok; ++i) {
-            if (!wait_warp(bar(L::bSFree + i), j & 1, abort_flag, p)) { ok = false; break; }
+      if constexpr (L::kMerged) {
+        for (int j = 0; ok && j < nb; ++j) {
+          const int st = j % L::kStages;
+          const int st2 = (j + 1) % L::kStages;
+          if (j + 1 < nb) {
+            // Scores of block j+1 once K_{j+1} has landed and both warpgroups
+            // have their block-j scores in registers.
+            if (!wait_warp(bar(L::bKFull + st2), ((j + 1) / L::kStages) & 1, abort_flag, p) ||
+                !wait_warp(bar(L::bSFree), j & 1, abort_flag, p))
+              break;
             ptx::tc_fence_after();
-            issue_s(i, st2);
+            for (int i = 0; i < kNumQ; ++i) issue_s(i, st2);
           }
-          if (!ok) break;
-        }
-        if (!wait_warp(bar(L::bVFull + st), (j / L::kStages) & 1, abort_flag, p)) break;
-        for (int i = 0; i < kNumQ; ++i) {
-          if (!wait_warp(bar(L::bPFull + i), j & 1, abort_flag, p)) { ok = false; break; }
+          // V_j landed with K_j; both warpgroups have written P(j)
+          if (!wait_warp(bar(L::bPFull), j & 1, abort_flag, p)) break;
           ptx::tc_fence_after();
-          issue_pv(i, st, j > 0);
-          if (i == kNumQ - 1 && leader) ptx::mma_commit(bar(L::bKVEmpty + st));
-          if (!L::kEarlyS && more) {
-            // P_i shares columns with S_i: the next scores go in only after
-            // O_i += P_i V_j (the tensor pipe runs one thread's MMAs in order).
-            if (i == 0) {
-              if (!wait_warp(bar(L::bKFull + st2), ((j + 1) / L::kStages) & 1,
-                             abort_flag, p)) { ok = false; break; }
+          for (int i = 0; i < kNumQ; ++i) issue_pv(i, st, j > 0);
+          if (leader) ptx::mma_commit(bar(L::bKVEmpty + st));
+        }
+      } else {
+        for (int j = 0; ok && j < nb; ++j) {
+          const int st = j % L::kStages;
+          const int st2 = (j + 1) % L::kStages;
+          const bool more = j + 1 < nb;
+          if (L::kEarlyS && more) {
+            // Scores of block j+1 as soon as each softmax warpgroup has its
+            // block-j scores in registers.
+            if (!wait_warp(bar(L::bKFull + st2), ((j + 1) / L::kStages) & 1, abort_flag, p)) break;
+            for (int i = 0; i < kNumQ && ok; ++i) {
+              if (!wait_warp(bar(L::bSFree + i), j & 1, abort_flag, p)) { ok = false; break; }
               ptx::tc_fence_after();
+              issue_s(i, st2);
             }
-            issue_s(i, st2);
+            if (!ok) break;
+          }
+          if (!wait_warp(bar(L::bVFull + st), (j / L::kStages) & 1, abort_flag, p)) break;
+          for (int i = 0; i < kNumQ; ++i) {
+            if (!wait_warp(bar(L::bPFull + i), j & 1, abort_flag, p)) { ok = false; break; }
+            ptx::tc_fence_after();
+            issue_pv(i, st, j > 0);
+            if (i == kNumQ - 1 && leader) ptx::mma_commit(bar(L::bKVEmpty + st));
+            if (!L::kEarlyS && more) {
+              // P_i shares columns with S_i: the next scores go in only after
+              // O_i += P_i V_j (the tensor pipe runs one thread's MMAs in order).
+              if (i == 0) {
+                if (!wait_warp(bar(L::bKFull + st2), ((j + 1) / L::kStages) & 1,
+                               abort_flag, p)) { ok = false; break; }
+                ptx::tc_fence_after();
+              }
+              issue_s(i, st2);
+            }
           }
         }
       }
@@ -455,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&s[cc * 32]));
       if (L::kEarlyS) {
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(L::bSFree + i));
+        ptx::mbar_arrive(bar(L::bSFree + (L::kMerged ? 0 : i)));
       }
       float *sf = reinterpret_cast<float *>(s);
 
@@ -545,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(L::bPFull + i));
+      ptx::mbar_arrive(bar(L::bPFull + (L::kMerged ? 0 : i)));
       const float2 r01 = __fadd2_rn(rs[0], rs[1]);
       const float2 r23 = __fadd2_rn(rs[2], rs[3]);
       l = l * alpha + ((r01.x + r01.y) + (r23.x + r23.y));
