@@ -56,7 +56,7 @@ DEFAULT_WORKLOAD = W.N8192.name
 # workload; reported only while the sources are unchanged (see
 # profiles/fa_fwd_kernel_b8h32n8192d64_bf16_launches.md).
 MEASURED_TRAFFIC = {
-    ("fa7fd3205794918a", "b8h32n8192d64_bf16"): 805.80e6 + 252.56e6,
+    ("32fd99c72a2f3d33", "b8h32n8192d64_bf16"): 805.62e6 + 254.00e6,
 }
 CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw",
                 "clocks_event_reasons.active",
