@@ -181,9 +181,9 @@ fa_status run_bwd(const void *q, const void *k, const void *v, const void *dout,
   if (!encode_map<D, T>(&mq, q, p.Nq, bh) || !encode_map<D, T>(&mk, k, p.Nk, bh) ||
       !encode_map<D, T>(&mv, v, p.Nk, bh) || !encode_map<D, T>(&mdo, dout, p.Nq, bh))
     return FA_ERR_CUDA;
-  const long long rows = bh * (long long)p.Nq;
-  const long long threads = rows * 8;
-  fa_bwd_dot_kernel<D, T><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(p, rows);
+  const long long rows_pad = bh * (long long)p.n_pad;
+  const long long threads = rows_pad * 8;
+  fa_bwd_dot_kernel<D, T><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(p, rows_pad);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kBwdThreads, 1, 1);
@@ -392,8 +392,10 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o,
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N) {
   if (B <= 0 || H <= 0 || N <= 0) return 0;
-  const size_t bytes = (size_t)B * (size_t)H * (size_t)N * sizeof(float);
-  return (bytes + 255) & ~(size_t)255;
+  // two fp32 arrays (LSE in exp2 units, D) of B*H heads x N rounded up to
+  // whole 128-row blocks
+  const size_t n_pad = ((size_t)N + fa::kBM - 1) / fa::kBM * fa::kBM;
+  return 2 * (size_t)B * (size_t)H * n_pad * sizeof(float);
 }
 
 fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
@@ -424,7 +426,9 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
   p.o = o;
   p.dout = dout;
   p.lse = lse;
-  p.dsum = static_cast<float *>(workspace);
+  p.n_pad = (N + kBM - 1) / kBM * kBM;
+  p.lse2 = static_cast<float *>(workspace);
+  p.dsum = p.lse2 + (size_t)bh * (size_t)p.n_pad;
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
@@ -503,10 +507,11 @@ fa_status fa_selftest_wait_timeout(unsigned long long timeout_ns,
 namespace fa {
 namespace {
 
-// Row sums D of fa_bwd_noalloc: static device memory (one copy on every
-// device that loads the library), shared by all calls.
+// Scratch of fa_bwd_noalloc (LSE in exp2 units and D, two fp32 per padded
+// query row): static device memory, one copy on every device that loads
+// the library, shared by all calls.
 constexpr long long kNoAllocMaxRows = FA_BWD_NOALLOC_MAX_ROWS;
-static __device__ __align__(256) float g_noalloc_dsum[kNoAllocMaxRows];
+static __device__ __align__(256) float g_noalloc_dsum[2 * kNoAllocMaxRows];
 
 std::mutex g_noalloc_mutex;
 void *g_noalloc_ptr[kMaxDevices] = {};
@@ -540,15 +545,15 @@ fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v,
   if (B == 0 || H == 0 || N == 0)   // empty problem: fa_bwd's checks, no scratch
     return fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, nullptr, 0, B, H, N, d,
                   causal, scale, dtype, stream);
-  if ((long long)B * (long long)H * (long long)N > kNoAllocMaxRows)
-    return FA_ERR_WORKSPACE;
+  const long long n_pad = ((long long)N + kBM - 1) / kBM * kBM;
+  if ((long long)B * (long long)H * n_pad > kNoAllocMaxRows) return FA_ERR_WORKSPACE;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   void *scratch = nullptr;
   const fa_status st = noalloc_scratch(dev, &scratch);
   if (st != FA_OK) return st;
   return fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, scratch,
-                (size_t)kNoAllocMaxRows * sizeof(float), B, H, N, d, causal,
+                2 * (size_t)kNoAllocMaxRows * sizeof(float), B, H, N, d, causal,
                 scale, dtype, stream);
 }
 

@@ -11,7 +11,10 @@
 // the backward recomputes P from Q, K and the stored LSE in the same way.
 //
 // Three kernels, no atomics:
-//   fa_bwd_dot_kernel   D for every query row (into the caller's workspace)
+//   fa_bwd_dot_kernel   D for every query row, and LSE in exp2 units, into
+//                       the workspace, each head padded to whole 128-row
+//                       blocks (D = 0 and LSE = +inf on padding, so its
+//                       probabilities are zero)
 //   fa_bwd_dq_kernel    one CTA per 128 query rows, looping over key blocks:
 //                       S = Q K^T and dP = dO V^T into TMEM, dS to TMEM,
 //                       dQ += dS K (K read as the MN-major B operand)
@@ -39,7 +42,9 @@ constexpr int kBwdHalf = 64;             // columns per element-wise thread
 struct BwdParams {
   const void *o, *dout;      // [BH, Nq, D]
   const float *lse;          // [BH, Nq]
-  float *dsum;               // D = rowsum(dO .* O), [BH, Nq] (workspace)
+  float *lse2;               // LSE * log2(e), +inf where no key is seen, [BH, n_pad] (workspace)
+  float *dsum;               // D = rowsum(dO .* O), [BH, n_pad] (workspace)
+  int n_pad;                 // Nq rounded up to whole 128-row blocks
   void *dq, *dk, *dv;        // outputs
   int Nq, Nk;
   int n_qblk, n_kblk;        // ceil(Nq / 128), ceil(Nk / 128)
@@ -51,15 +56,20 @@ struct BwdParams {
 };
 
 // ---------------------------------------------------------------- D
-// Eight lanes per row, each with D/8 consecutive elements (16-byte loads).
+// Eight lanes per padded row, each with D/8 consecutive elements (16-byte
+// loads); lane 0 also converts the row's LSE to exp2 units.
 template <int D, int T>
 __global__ void __launch_bounds__(256)
-    fa_bwd_dot_kernel(const BwdParams p, long long rows) {
+    fa_bwd_dot_kernel(const BwdParams p, long long rows_pad) {
   const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long row = gid >> 3;
+  const long long prow = gid >> 3;                 // padded row
   const int part = (int)(gid & 7);
+  const long long bh = prow / p.n_pad;
+  const int i = (int)(prow - bh * p.n_pad);
+  const bool valid = prow < rows_pad && i < p.Nq;
+  const long long row = bh * p.Nq + i;             // row of o, dout, lse
   float acc = 0.f;
-  if (row < rows) {
+  if (valid) {
     const uint4 *o = reinterpret_cast<const uint4 *>(
         reinterpret_cast<const uint16_t *>(p.o) + row * D + part * (D / 8));
     const uint4 *g = reinterpret_cast<const uint4 *>(
@@ -86,7 +96,16 @@ __global__ void __launch_bounds__(256)
   acc += __shfl_xor_sync(0xffffffffu, acc, 1);
   acc += __shfl_xor_sync(0xffffffffu, acc, 2);
   acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-  if (row < rows && part == 0) p.dsum[row] = acc;
+  if (prow < rows_pad && part == 0) {
+    float l2 = CUDART_INF_F;
+    if (valid) {
+      // a row that sees no key has LSE = -inf: its probabilities are zero
+      const float lse = p.lse[row];
+      l2 = lse == -CUDART_INF_F ? CUDART_INF_F : lse * 1.4426950408889634f;
+    }
+    p.lse2[prow] = l2;
+    p.dsum[prow] = valid ? acc : 0.f;
+  }
 }
 
 // ---------------------------------------------------------------- layouts
@@ -94,7 +113,11 @@ template <int D, int T>
 struct BwdQLayout {
   using F = Layout<D, T>;
   static constexpr int kTile = F::kTileBytes;
-  static constexpr int kStages = kTile <= 16384 ? 3 : 2;
+  // D = 64: four stages, K and V of a stage on one barrier, and one "S and
+  // dP read" wait per block gating both the next S, dP and the previous
+  // block's dQ product (the loads then have two blocks of lead time).
+  static constexpr bool kMerged = kTile <= 16384;
+  static constexpr int kStages = kMerged ? 4 : 2;
   static constexpr int kQ = 0;                           // Q tile
   static constexpr int kdO = kTile;                      // dO tile
   static constexpr int kK = 2 * kTile;                   // K ring
@@ -122,7 +145,7 @@ struct BwdKVLayout {
   using F = Layout<D, T>;
   static constexpr int kTile = F::kTileBytes;
   static constexpr int kStageBytes = 2 * kTile + 2 * kBM * 4;   // Q, dO, LSE, D
-  static constexpr int kStages = kTile <= 16384 ? 3 : 2;
+  static constexpr int kStages = kTile <= 16384 ? 4 : 2;
   static constexpr int kK = 0, kV = kTile;
   static constexpr int kStage0 = 2 * kTile;
   static constexpr int kBars = kStage0 + kStages * kStageBytes;
@@ -238,13 +261,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int st = j % L::kStages, use = j / L::kStages;
         if (use > 0 && !wait_warp(bar(L::bKVEmpty + st), (use - 1) & 1, abort_flag, p)) break;
         if (leader) {
-          ptx::mbar_arrive_expect_tx(bar(L::bKFull + st), L::kTile);
-          ptx::mbar_arrive_expect_tx(bar(L::bVFull + st), L::kTile);
+          const uint32_t vbar = bar(L::kMerged ? L::bKFull + st : L::bVFull + st);
+          ptx::mbar_arrive_expect_tx(bar(L::bKFull + st), L::kMerged ? 2 * L::kTile : L::kTile);
+          if (!L::kMerged) ptx::mbar_arrive_expect_tx(vbar, L::kTile);
           for (int c = 0; c < F::kChunks; ++c) {
             ptx::tma_load_3d(sbase + L::kK + st * L::kTile + c * F::kChunkBytes, &tmK,
                              bar(L::bKFull + st), c * F::kChunkElems, j * kBN, bh, pol_kv);
             ptx::tma_load_3d(sbase + L::kV + st * L::kTile + c * F::kChunkBytes, &tmV,
-                             bar(L::bVFull + st), c * F::kChunkElems, j * kBN, bh, pol_kv);
+                             vbar, c * F::kChunkElems, j * kBN, bh, pol_kv);
           }
         }
         issued = j + 1;
@@ -255,7 +279,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int st = j % L::kStages;
         const uint32_t ph = (uint32_t)(j / L::kStages) & 1u;
         wait_drain(bar(L::bKFull + st), ph, p);
-        wait_drain(bar(L::bVFull + st), ph, p);
+        if (!L::kMerged) wait_drain(bar(L::bVFull + st), ph, p);
       }
     }
   } else if (warp == kBwdMmaWarp) {
@@ -298,12 +322,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
       bool ok = wait_warp(bar(L::bQFull), 0, abort_flag, p) &&
                 wait_warp(bar(L::bKFull), 0, abort_flag, p) &&
-                wait_warp(bar(L::bVFull), 0, abort_flag, p);
+                (L::kMerged || wait_warp(bar(L::bVFull), 0, abort_flag, p));
       if (ok) {
         ptx::tc_fence_after();
         issue_s(0);
       }
-      for (int j = 0; ok && j < nb; ++j) {
+      if constexpr (L::kMerged) {
+        for (int j = 0; ok && j < nb; ++j) {
+          const int st2 = (j + 1) % L::kStages;
+          if (j + 1 < nb &&
+              !wait_warp(bar(L::bKFull + st2), ((j + 1) / L::kStages) & 1, abort_flag, p)) {
+            ok = false;
+            break;
+          }
+          // S(j), dP(j) are in registers; dS(j-1) was written before that
+          if (!wait_warp(bar(L::bSFree), j & 1, abort_flag, p)) { ok = false; break; }
+          ptx::tc_fence_after();
+          if (j + 1 < nb) issue_s(st2);
+          if (j > 0) issue_dq((j - 1) % L::kStages, (j - 1) & 1, j > 1);
+        }
+        // the last block's dQ product once its dS is written
+        if (ok && wait_warp(bar(L::bDSFull), 0, abort_flag, p)) {
+          ptx::tc_fence_after();
+          issue_dq((nb - 1) % L::kStages, (nb - 1) & 1, nb > 1);
+        }
+      }
+      for (int j = 0; !L::kMerged && ok && j < nb; ++j) {
         const int st = j % L::kStages, st2 = (j + 1) % L::kStages;
         if (j + 1 < nb) {
           const uint32_t ph2 = ((j + 1) / L::kStages) & 1;
@@ -329,13 +373,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool valid = row < p.Nq;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const size_t grow = (size_t)bh * (size_t)p.Nq + (size_t)row;
-    float lse_l2 = 0.f, dsum = 0.f;
-    if (valid) {
-      const float lse = p.lse[grow];
-      // a row that sees no key has LSE = -inf: its probabilities are zero
-      lse_l2 = lse == -CUDART_INF_F ? CUDART_INF_F : lse * 1.4426950408889634f;
-      dsum = p.dsum[grow];
-    }
+    const size_t prow = (size_t)bh * (size_t)p.n_pad + (size_t)row;   // row < n_pad
+    const float lse_l2 = p.lse2[prow], dsum = p.dsum[prow];
     const int key_lim = p.causal ? min(p.Nk, row + 1 + (p.Nk - p.Nq)) : p.Nk;
     const float c = p.c;
     bool ok = true;
@@ -343,39 +382,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int b = j & 1;
       if (!wait_warp(bar(L::bSFull), j & 1, abort_flag, p)) { ok = false; break; }
       ptx::tc_fence_after();
+      // S and dP of this half into registers first, so that the next
+      // block's S and dP products overlap this block's element-wise work
+      uint32_t s[kBwdHalf], dp[kBwdHalf];
+#pragma unroll
+      for (int cc = 0; cc < kBwdHalf; cc += 32) {
+        ptx::tmem_ld32(tmem + lane_off + L::tS + h * kBwdHalf + cc,
+                       *reinterpret_cast<uint32_t(*)[32]>(&s[cc]));
+        ptx::tmem_ld32(tmem + lane_off + L::tdP + h * kBwdHalf + cc,
+                       *reinterpret_cast<uint32_t(*)[32]>(&dp[cc]));
+      }
+      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int cc = 0; cc < kBwdHalf; cc += 32) {
+        ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&s[cc]));
+        ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&dp[cc]));
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(L::bSFree));
+      const int lim = key_lim - j * kBN - h * kBwdHalf;   // this half's columns >= lim: masked
+      uint32_t pk[kBwdHalf / 2];
+#pragma unroll
+      for (int t = 0; t < kBwdHalf; t += 2) {
+        float pr0 = ptx::ex2_approx(fmaf(__uint_as_float(s[t]), c, -lse_l2));
+        float pr1 = ptx::ex2_approx(fmaf(__uint_as_float(s[t + 1]), c, -lse_l2));
+        if (t >= lim) pr0 = 0.f;
+        if (t + 1 >= lim) pr1 = 0.f;
+        const float ds0 = pr0 * (__uint_as_float(dp[t]) - dsum);
+        const float ds1 = pr1 * (__uint_as_float(dp[t + 1]) - dsum);
+        pk[t / 2] = pack2<T>(ds0, ds1);
+      }
       if (j >= 2) {
         // dQ += dS_b K of two blocks back has finished reading dS_b
         if (!wait_warp(bar(L::bDQDone + b), ((j - 2) >> 1) & 1, abort_flag, p)) { ok = false; break; }
         ptx::tc_fence_after();
       }
-      const int lim = key_lim - j * kBN - h * kBwdHalf;   // this half's columns >= lim: masked
-      uint32_t pk[kBwdHalf / 2];
-#pragma unroll
-      for (int cc = 0; cc < kBwdHalf; cc += 32) {
-        uint32_t s[32], dp[32];
-        ptx::tmem_ld32(tmem + lane_off + L::tS + h * kBwdHalf + cc, s);
-        ptx::tmem_ld32(tmem + lane_off + L::tdP + h * kBwdHalf + cc, dp);
-        ptx::tmem_wait_ld();
-        ptx::reg_fence32(s);
-        ptx::reg_fence32(dp);
-#pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          float pr0 = ptx::ex2_approx(fmaf(__uint_as_float(s[t]), c, -lse_l2));
-          float pr1 = ptx::ex2_approx(fmaf(__uint_as_float(s[t + 1]), c, -lse_l2));
-          if (cc + t >= lim) pr0 = 0.f;
-          if (cc + t + 1 >= lim) pr1 = 0.f;
-          const float ds0 = pr0 * (__uint_as_float(dp[t]) - dsum);
-          const float ds1 = pr1 * (__uint_as_float(dp[t + 1]) - dsum);
-          pk[(cc + t) / 2] = pack2<T>(ds0, ds1);
-        }
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(L::bSFree));
       ptx::tmem_st32(tmem + lane_off + L::tdS(b) + h * (kBwdHalf / 2),
                      *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(L::bDSFull));
+      // (merged: the MMA thread learns of dS(j) from the next S-read
+      // arrival, so only the last block's dS is announced here)
+      if (!L::kMerged || j == nb - 1) ptx::mbar_arrive(bar(L::bDSFull));
     }
     // ---- epilogue: dQ = scale * (dS K), this half's columns
     if (ok && nb > 0)
@@ -455,7 +503,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(L::bKVFull), 1);
     for (int s = 0; s < L::kStages; ++s) {
-      ptx::mbar_init(bar(L::bQFull + s), 1 + 32);    // TMA bytes + 32 lanes' LSE/D
+      ptx::mbar_init(bar(L::bQFull + s), 1);         // Q, dO tiles and LSE, D rows
       ptx::mbar_init(bar(L::bQEmpty + s), 1);
     }
     ptx::mbar_init(bar(L::bSFull), 1);
@@ -493,31 +541,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (use > 0 && !wait_warp(bar(L::bQEmpty + st), (use - 1) & 1, abort_flag, p)) break;
         const uint32_t sa = sbase + L::stage(st);
         if (leader) {
-          ptx::mbar_arrive_expect_tx(bar(L::bQFull + st), 2 * L::kTile);
+          ptx::mbar_arrive_expect_tx(bar(L::bQFull + st), 2 * L::kTile + 2 * kBM * 4);
           for (int c = 0; c < F::kChunks; ++c) {
             ptx::tma_load_3d(sa + c * F::kChunkBytes, &tmQ, bar(L::bQFull + st),
                              c * F::kChunkElems, i * kBM, bh, pol_q);
             ptx::tma_load_3d(sa + L::kTile + c * F::kChunkBytes, &tmdO,
                              bar(L::bQFull + st), c * F::kChunkElems, i * kBM, bh, pol_q);
           }
+          // the block's 128 rows of LSE (exp2 units) and D: whole padded rows
+          const size_t prow = (size_t)bh * (size_t)p.n_pad + (size_t)i * kBM;
+          ptx::bulk_load(sa + 2 * L::kTile, p.lse2 + prow, kBM * 4, bar(L::bQFull + st), pol_q);
+          ptx::bulk_load(sa + 2 * L::kTile + kBM * 4, p.dsum + prow, kBM * 4,
+                         bar(L::bQFull + st), pol_q);
         }
-        // per query row of the block: LSE in exp2 units (+inf where the row
-        // is past Nq or sees no key, giving zero probabilities) and D
-        float *lse_s = reinterpret_cast<float *>(sm.smem + L::stage(st) + 2 * L::kTile);
-        float *d_s = lse_s + kBM;
-        for (int t = lane; t < kBM; t += 32) {
-          const int row = i * kBM + t;
-          float l2 = CUDART_INF_F, dd = 0.f;
-          if (row < p.Nq) {
-            const size_t g = (size_t)bh * (size_t)p.Nq + (size_t)row;
-            const float lse = p.lse[g];
-            l2 = lse == -CUDART_INF_F ? CUDART_INF_F : lse * 1.4426950408889634f;
-            dd = p.dsum[g];
-          }
-          lse_s[t] = l2;
-          d_s[t] = dd;
-        }
-        ptx::mbar_arrive(bar(L::bQFull + st));
         issued = n + 1;
       }
       wait_drain(bar(L::bKVFull), 0, p);
@@ -573,7 +609,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ptx::tc_fence_after();
         issue_s(0);
       }
-      for (int n = 0; ok && n < nqb; ++n) {
+      if constexpr (L::kEarly) {
+        for (int n = 0; ok && n < nqb; ++n) {
+          const int st2 = (n + 1) % L::kStages;
+          if (n + 1 < nqb &&
+              !wait_warp(bar(L::bQFull + st2), ((n + 1) / L::kStages) & 1, abort_flag, p)) {
+            ok = false;
+            break;
+          }
+          // S^T(n), dP^T(n) are in registers; P^T(n-1), dS^T(n-1) were
+          // written before that.  The gradient products of block n-1 go
+          // first: the element-wise warps wait for them before their next
+          // P^T store.
+          if (!wait_warp(bar(L::bSFree), n & 1, abort_flag, p)) { ok = false; break; }
+          ptx::tc_fence_after();
+          if (n > 0) issue_g((n - 1) % L::kStages, n > 1);
+          if (n + 1 < nqb) issue_s(st2);
+        }
+        if (ok && wait_warp(bar(L::bPFull), 0, abort_flag, p)) {
+          ptx::tc_fence_after();
+          issue_g((nqb - 1) % L::kStages, nqb > 1);
+        }
+      }
+      for (int n = 0; !L::kEarly && ok && n < nqb; ++n) {
         const int st = n % L::kStages, st2 = (n + 1) % L::kStages;
         const uint32_t ph2 = ((n + 1) / L::kStages) & 1;
         const bool more = n + 1 < nqb;
@@ -621,35 +679,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float *d_s = lse_s + kBM;
       // columns (query rows) of this half before `first` do not see the key
       const int first = p.causal ? key - shift - i * kBM - h * kBwdHalf : 0;
-      uint32_t pkp[kBwdHalf / 2], pkd[kBwdHalf / 2];
+      // S^T and dP^T of this half into registers first, so that the next
+      // block's products overlap this block's element-wise work
+      uint32_t s[kBwdHalf], dp[kBwdHalf];
 #pragma unroll
       for (int cc = 0; cc < kBwdHalf; cc += 32) {
-        uint32_t s[32], dp[32];
-        ptx::tmem_ld32(tmem + lane_off + L::tS + h * kBwdHalf + cc, s);
-        ptx::tmem_ld32(tmem + lane_off + L::tdP + h * kBwdHalf + cc, dp);
-        ptx::tmem_wait_ld();
-        ptx::reg_fence32(s);
-        ptx::reg_fence32(dp);
+        ptx::tmem_ld32(tmem + lane_off + L::tS + h * kBwdHalf + cc,
+                       *reinterpret_cast<uint32_t(*)[32]>(&s[cc]));
+        ptx::tmem_ld32(tmem + lane_off + L::tdP + h * kBwdHalf + cc,
+                       *reinterpret_cast<uint32_t(*)[32]>(&dp[cc]));
+      }
+      ptx::tmem_wait_ld();
 #pragma unroll
-        for (int t = 0; t < 32; t += 4) {
-          const float4 l4 = *reinterpret_cast<const float4 *>(lse_s + cc + t);
-          const float4 d4 = *reinterpret_cast<const float4 *>(d_s + cc + t);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pr[4], ds[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            pr[u] = ptx::ex2_approx(fmaf(__uint_as_float(s[t + u]), c, -lv[u]));
-            if (cc + t + u < first) pr[u] = 0.f;
-            ds[u] = pr[u] * (__uint_as_float(dp[t + u]) - dv4[u]);
-          }
-          pkp[(cc + t) / 2] = pack2<T>(pr[0], pr[1]);
-          pkp[(cc + t) / 2 + 1] = pack2<T>(pr[2], pr[3]);
-          pkd[(cc + t) / 2] = pack2<T>(ds[0], ds[1]);
-          pkd[(cc + t) / 2 + 1] = pack2<T>(ds[2], ds[3]);
-        }
+      for (int cc = 0; cc < kBwdHalf; cc += 32) {
+        ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&s[cc]));
+        ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&dp[cc]));
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(L::bSFree));
+      uint32_t pkp[kBwdHalf / 2], pkd[kBwdHalf / 2];
+#pragma unroll
+      for (int t = 0; t < kBwdHalf; t += 4) {
+        const float4 l4 = *reinterpret_cast<const float4 *>(lse_s + t);
+        const float4 d4 = *reinterpret_cast<const float4 *>(d_s + t);
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+        float pr[4], ds[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          pr[u] = ptx::ex2_approx(fmaf(__uint_as_float(s[t + u]), c, -lv[u]));
+          if (t + u < first) pr[u] = 0.f;
+          ds[u] = pr[u] * (__uint_as_float(dp[t + u]) - dv4[u]);
+        }
+        pkp[t / 2] = pack2<T>(pr[0], pr[1]);
+        pkp[t / 2 + 1] = pack2<T>(pr[2], pr[3]);
+        pkd[t / 2] = pack2<T>(ds[0], ds[1]);
+        pkd[t / 2 + 1] = pack2<T>(ds[2], ds[3]);
+      }
       if (n > 0) {
         // the gradient MMAs of the previous block have read P^T and dS^T
         if (!wait_warp(bar(L::bPDone), (n - 1) & 1, abort_flag, p)) { ok = false; break; }
@@ -661,7 +726,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                      *reinterpret_cast<uint32_t(*)[32]>(&pkd[0]));
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(L::bPFull));
+      // (early layout: the MMA thread learns of P^T(n) from the next S-read
+      // arrival, so only the last block's is announced here)
+      if (!L::kEarly || n == nqb - 1) ptx::mbar_arrive(bar(L::bPFull));
     }
     // ---- epilogue: dV and dK = scale * (dS^T Q), this half's columns
     if (ok && nqb > 0) ok = wait_warp(bar(L::bPDone), (nqb - 1) & 1, abort_flag, p);

@@ -159,8 +159,10 @@ FA_API fa_status fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
                              fa_dtype dtype, fa_stream_t stream);
 
 /*
- * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs for
- * B*H*N query rows (one fp32 per row, rounded up to 256 bytes).
+ * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs: two
+ * fp32 per query row (the row's logsumexp in base-2 units and
+ * D = rowsum(dout .* o)), each head's N rows rounded up to a multiple of
+ * 128: 8 * B * H * ceil(N / 128) * 128 bytes.  0 for an empty problem.
  */
 FA_API size_t fa_bwd_workspace_bytes(int B, int H, int N);
 
@@ -199,10 +201,10 @@ FA_API fa_status fa_bwd(const void *q, const void *k, const void *v,
  * fixed array in the library's static device memory instead, so it takes no
  * workspace argument and allocates nothing.
  *
- * Limit: B * H * N <= FA_BWD_NOALLOC_MAX_ROWS (2^21, one fp32 per query
- * row: 8 MiB held on every device that loads the library, until the
- * process exits).  Larger problems return FA_ERR_WORKSPACE without touching
- * the device; use fa_bwd with a workspace for them.
+ * Limit: B * H * ceil(N / 128) * 128 <= FA_BWD_NOALLOC_MAX_ROWS (2^21;
+ * two fp32 per row: 16 MiB held on every device that loads the library,
+ * until the process exits).  Larger problems return FA_ERR_WORKSPACE
+ * without touching the device; use fa_bwd with a workspace for them.
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream

@@ -128,8 +128,10 @@ def test_bwd_matches_torch_autograd_direction():
 
 # ---------------------------------------------------------------- host side
 def test_bwd_workspace_size_and_checks():
-    assert fa.bwd_workspace_bytes(1, 1, 1) == 256
-    assert fa.bwd_workspace_bytes(8, 32, 8192) == 8 * 32 * 8192 * 4
+    # two fp32 per query row, each head padded to whole 128-row blocks
+    assert fa.bwd_workspace_bytes(1, 1, 1) == 2 * 128 * 4
+    assert fa.bwd_workspace_bytes(1, 1, 129) == 2 * 256 * 4
+    assert fa.bwd_workspace_bytes(8, 32, 8192) == 2 * 8 * 32 * 8192 * 4
     assert fa.bwd_workspace_bytes(0, 1, 1) == 0
     P = 0x10000
     import ctypes
@@ -142,6 +144,7 @@ def test_bwd_workspace_size_and_checks():
                             a["d"], 1, a["scale"], a["dtype"], ctypes.c_void_p(0))
     assert call(ws=0) == b.FA_ERR_WORKSPACE
     assert call(wsb=16) == b.FA_ERR_WORKSPACE
+    assert call(wsb=2 * 128 * 4 - 4) == b.FA_ERR_WORKSPACE
     assert call(ws=P + 4) == b.FA_ERR_WORKSPACE
     assert call(d=96) == b.FA_ERR_HEADDIM
     assert call(dtype=7) == b.FA_ERR_DTYPE
