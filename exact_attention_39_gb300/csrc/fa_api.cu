@@ -427,8 +427,8 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
   p.dout = dout;
   p.lse = lse;
   p.n_pad = (N + kBM - 1) / kBM * kBM;
-  p.lse2 = static_cast<float *>(workspace);
-  p.dsum = p.lse2 + (size_t)bh * (size_t)p.n_pad;
+  p.nlse2 = static_cast<float *>(workspace);
+  p.ndsum = p.nlse2 + (size_t)bh * (size_t)p.n_pad;
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;

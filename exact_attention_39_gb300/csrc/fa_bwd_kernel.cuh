@@ -11,10 +11,11 @@
 // the backward recomputes P from Q, K and the stored LSE in the same way.
 //
 // Three kernels, no atomics:
-//   fa_bwd_dot_kernel   D for every query row, and LSE in exp2 units, into
+//   fa_bwd_dot_kernel   -D for every query row, and -LSE in exp2 units, into
 //                       the workspace, each head padded to whole 128-row
-//                       blocks (D = 0 and LSE = +inf on padding, so its
-//                       probabilities are zero)
+//                       blocks (0 and -inf on padding, so its probabilities
+//                       are zero); negated so that the element-wise steps
+//                       are packed two-wide adds and fused multiply-adds
 //   fa_bwd_dq_kernel    one CTA per 128 query rows, looping over key blocks:
 //                       S = Q K^T and dP = dO V^T into TMEM, dS to TMEM,
 //                       dQ += dS K (K read as the MN-major B operand)
@@ -29,6 +30,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
@@ -42,8 +45,8 @@ constexpr int kBwdHalf = 64;             // columns per element-wise thread
 struct BwdParams {
   const void *o, *dout;      // [BH, Nq, D]
   const float *lse;          // [BH, Nq]
-  float *lse2;               // LSE * log2(e), +inf where no key is seen, [BH, n_pad] (workspace)
-  float *dsum;               // D = rowsum(dO .* O), [BH, n_pad] (workspace)
+  float *nlse2;              // -LSE * log2(e), -inf where no key is seen, [BH, n_pad] (workspace)
+  float *ndsum;              // -D = -rowsum(dO .* O), [BH, n_pad] (workspace)
   int n_pad;                 // Nq rounded up to whole 128-row blocks
   void *dq, *dk, *dv;        // outputs
   int Nq, Nk;
@@ -97,14 +100,14 @@ __global__ void __launch_bounds__(256)
   acc += __shfl_xor_sync(0xffffffffu, acc, 2);
   acc += __shfl_xor_sync(0xffffffffu, acc, 4);
   if (prow < rows_pad && part == 0) {
-    float l2 = CUDART_INF_F;
+    float nl2 = -CUDART_INF_F;
     if (valid) {
       // a row that sees no key has LSE = -inf: its probabilities are zero
       const float lse = p.lse[row];
-      l2 = lse == -CUDART_INF_F ? CUDART_INF_F : lse * 1.4426950408889634f;
+      nl2 = lse == -CUDART_INF_F ? -CUDART_INF_F : -lse * 1.4426950408889634f;
     }
-    p.lse2[prow] = l2;
-    p.dsum[prow] = valid ? acc : 0.f;
+    p.nlse2[prow] = nl2;
+    p.ndsum[prow] = valid ? -acc : 0.f;
   }
 }
 
@@ -374,9 +377,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const size_t grow = (size_t)bh * (size_t)p.Nq + (size_t)row;
     const size_t prow = (size_t)bh * (size_t)p.n_pad + (size_t)row;   // row < n_pad
-    const float lse_l2 = p.lse2[prow], dsum = p.dsum[prow];
+    const float nl2 = p.nlse2[prow], nd = p.ndsum[prow];
+    const float2 nl2x2 = make_float2(nl2, nl2), ndx2 = make_float2(nd, nd);
     const int key_lim = p.causal ? min(p.Nk, row + 1 + (p.Nk - p.Nq)) : p.Nk;
     const float c = p.c;
+    const float2 c2 = make_float2(c, c);
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
       const int b = j & 1;
@@ -402,16 +407,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::mbar_arrive(bar(L::bSFree));
       const int lim = key_lim - j * kBN - h * kBwdHalf;   // this half's columns >= lim: masked
       uint32_t pk[kBwdHalf / 2];
+      // dS = P .* (dP - D), two columns at a time; the mask test only on
+      // blocks where some row of the warp has masked columns
+      auto ds_block = [&](auto mask_tag) {
+        constexpr bool kMask = decltype(mask_tag)::value;
 #pragma unroll
-      for (int t = 0; t < kBwdHalf; t += 2) {
-        float pr0 = ptx::ex2_approx(fmaf(__uint_as_float(s[t]), c, -lse_l2));
-        float pr1 = ptx::ex2_approx(fmaf(__uint_as_float(s[t + 1]), c, -lse_l2));
-        if (t >= lim) pr0 = 0.f;
-        if (t + 1 >= lim) pr1 = 0.f;
-        const float ds0 = pr0 * (__uint_as_float(dp[t]) - dsum);
-        const float ds1 = pr1 * (__uint_as_float(dp[t + 1]) - dsum);
-        pk[t / 2] = pack2<T>(ds0, ds1);
-      }
+        for (int t = 0; t < kBwdHalf; t += 2) {
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(s[t]), __uint_as_float(s[t + 1])),
+                                      c2, nl2x2);
+          float2 pr = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+          if (kMask) {
+            if (t >= lim) pr.x = 0.f;
+            if (t + 1 >= lim) pr.y = 0.f;
+          }
+          const float2 g = __fadd2_rn(make_float2(__uint_as_float(dp[t]), __uint_as_float(dp[t + 1])),
+                                      ndx2);
+          const float2 ds = __fmul2_rn(pr, g);
+          pk[t / 2] = pack2<T>(ds.x, ds.y);
+        }
+      };
+      if (__any_sync(0xffffffffu, lim < kBwdHalf))
+        ds_block(std::true_type{});
+      else
+        ds_block(std::false_type{});
       if (j >= 2) {
         // dQ += dS_b K of two blocks back has finished reading dS_b
         if (!wait_warp(bar(L::bDQDone + b), ((j - 2) >> 1) & 1, abort_flag, p)) { ok = false; break; }
@@ -550,8 +568,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           // the block's 128 rows of LSE (exp2 units) and D: whole padded rows
           const size_t prow = (size_t)bh * (size_t)p.n_pad + (size_t)i * kBM;
-          ptx::bulk_load(sa + 2 * L::kTile, p.lse2 + prow, kBM * 4, bar(L::bQFull + st), pol_q);
-          ptx::bulk_load(sa + 2 * L::kTile + kBM * 4, p.dsum + prow, kBM * 4,
+          ptx::bulk_load(sa + 2 * L::kTile, p.nlse2 + prow, kBM * 4, bar(L::bQFull + st), pol_q);
+          ptx::bulk_load(sa + 2 * L::kTile + kBM * 4, p.ndsum + prow, kBM * 4,
                          bar(L::bQFull + st), pol_q);
         }
         issued = n + 1;
@@ -663,6 +681,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int key = k0 + r;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const float c = p.c;
+    const float2 c2 = make_float2(c, c);
     const int shift = p.Nk - p.Nq;                  // causal: key <= row + shift
     bool ok = true;
     for (int n = 0; n < nqb; ++n) {
@@ -698,23 +717,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(L::bSFree));
       uint32_t pkp[kBwdHalf / 2], pkd[kBwdHalf / 2];
+      // P^T and dS^T = P^T .* (dP^T - D), two columns at a time (the
+      // staged rows hold -LSE in exp2 units and -D); the causal test only on
+      // blocks where some key of the warp has masked columns
+      auto p_block = [&](auto mask_tag) {
+        constexpr bool kMask = decltype(mask_tag)::value;
 #pragma unroll
-      for (int t = 0; t < kBwdHalf; t += 4) {
-        const float4 l4 = *reinterpret_cast<const float4 *>(lse_s + t);
-        const float4 d4 = *reinterpret_cast<const float4 *>(d_s + t);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-        float pr[4], ds[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          pr[u] = ptx::ex2_approx(fmaf(__uint_as_float(s[t + u]), c, -lv[u]));
-          if (t + u < first) pr[u] = 0.f;
-          ds[u] = pr[u] * (__uint_as_float(dp[t + u]) - dv4[u]);
+        for (int t = 0; t < kBwdHalf; t += 4) {
+          const float4 l4 = *reinterpret_cast<const float4 *>(lse_s + t);
+          const float4 d4 = *reinterpret_cast<const float4 *>(d_s + t);
+          const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(s[t]), __uint_as_float(s[t + 1])),
+                                       c2, make_float2(l4.x, l4.y));
+          const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(s[t + 2]), __uint_as_float(s[t + 3])),
+                                       c2, make_float2(l4.z, l4.w));
+          float2 p0 = make_float2(ptx::ex2_approx(x0.x), ptx::ex2_approx(x0.y));
+          float2 p1 = make_float2(ptx::ex2_approx(x1.x), ptx::ex2_approx(x1.y));
+          if (kMask) {
+            if (t < first) p0.x = 0.f;
+            if (t + 1 < first) p0.y = 0.f;
+            if (t + 2 < first) p1.x = 0.f;
+            if (t + 3 < first) p1.y = 0.f;
+          }
+          const float2 g0 = __fadd2_rn(make_float2(__uint_as_float(dp[t]), __uint_as_float(dp[t + 1])),
+                                       make_float2(d4.x, d4.y));
+          const float2 g1 = __fadd2_rn(make_float2(__uint_as_float(dp[t + 2]), __uint_as_float(dp[t + 3])),
+                                       make_float2(d4.z, d4.w));
+          const float2 ds0 = __fmul2_rn(p0, g0), ds1 = __fmul2_rn(p1, g1);
+          pkp[t / 2] = pack2<T>(p0.x, p0.y);
+          pkp[t / 2 + 1] = pack2<T>(p1.x, p1.y);
+          pkd[t / 2] = pack2<T>(ds0.x, ds0.y);
+          pkd[t / 2 + 1] = pack2<T>(ds1.x, ds1.y);
         }
-        pkp[t / 2] = pack2<T>(pr[0], pr[1]);
-        pkp[t / 2 + 1] = pack2<T>(pr[2], pr[3]);
-        pkd[t / 2] = pack2<T>(ds[0], ds[1]);
-        pkd[t / 2 + 1] = pack2<T>(ds[2], ds[3]);
-      }
+      };
+      if (__any_sync(0xffffffffu, first > 0))
+        p_block(std::true_type{});
+      else
+        p_block(std::false_type{});
       if (n > 0) {
         // the gradient MMAs of the previous block have read P^T and dS^T
         if (!wait_warp(bar(L::bPDone), (n - 1) & 1, abort_flag, p)) { ok = false; break; }
