@@ -301,10 +301,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t dk = dk0 + (uint64_t)((st * L::kTile) >> 4);
         const uint64_t dv = dv0 + (uint64_t)((st * L::kTile) >> 4);
         if (leader) {
+          // all of S's steps, then all of dP's (one accumulator at a time)
 #pragma unroll
           for (int kk = 0; kk < D / E::kMmaK; ++kk) {
             const uint32_t off = ((kk >> 2) * F::kChunkBytes + (kk & 3) * 32) >> 4;
             ptx::mma_ss(tmem + L::tS, dq_ + off, dk + off, idesc_s, kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / E::kMmaK; ++kk) {
+            const uint32_t off = ((kk >> 2) * F::kChunkBytes + (kk & 3) * 32) >> 4;
             ptx::mma_ss(tmem + L::tdP, ddo + off, dv + off, idesc_s, kk > 0);
           }
           ptx::mma_commit(bar(L::bSFull));
@@ -594,10 +599,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t dq_ = make_sdesc(sa, 16, F::kSBO, F::kSwzMode);
         const uint64_t ddo = make_sdesc(sa + L::kTile, 16, F::kSBO, F::kSwzMode);
         if (leader) {
+          // all of S^T's steps, then all of dP^T's
 #pragma unroll
           for (int kk = 0; kk < D / E::kMmaK; ++kk) {
             const uint32_t off = ((kk >> 2) * F::kChunkBytes + (kk & 3) * 32) >> 4;
             ptx::mma_ss(tmem + L::tS, dk + off, dq_ + off, idesc_s, kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / E::kMmaK; ++kk) {
+            const uint32_t off = ((kk >> 2) * F::kChunkBytes + (kk & 3) * 32) >> 4;
             ptx::mma_ss(tmem + L::tdP, dv + off, ddo + off, idesc_s, kk > 0);
           }
           ptx::mma_commit(bar(L::bSFull));
@@ -610,13 +620,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t dq_mn = make_sdesc(sa, F::kChunkBytes, F::kSBO, F::kSwzMode);
         const uint64_t ddo_mn = make_sdesc(sa + L::kTile, F::kChunkBytes, F::kSBO, F::kSwzMode);
         if (leader) {
+          // all of dV's steps, then all of dK's (one accumulator at a time)
 #pragma unroll
-          for (int kk = 0; kk < kBM / E::kMmaK; ++kk) {
-            const uint64_t off = (uint64_t)((kk * E::kMmaK * F::kSwz) >> 4);
-            const uint32_t a = (acc || kk > 0) ? 1u : 0u;
-            ptx::mma_ts(tmem + L::tdV, tmem + L::tP + kk * 8, ddo_mn + off, idesc_g, a);
-            ptx::mma_ts(tmem + L::tdK, tmem + L::tdS + kk * 8, dq_mn + off, idesc_g, a);
-          }
+          for (int kk = 0; kk < kBM / E::kMmaK; ++kk)
+            ptx::mma_ts(tmem + L::tdV, tmem + L::tP + kk * 8,
+                        ddo_mn + (uint64_t)((kk * E::kMmaK * F::kSwz) >> 4), idesc_g,
+                        (acc || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < kBM / E::kMmaK; ++kk)
+            ptx::mma_ts(tmem + L::tdK, tmem + L::tdS + kk * 8,
+                        dq_mn + (uint64_t)((kk * E::kMmaK * F::kSwz) >> 4), idesc_g,
+                        (acc || kk > 0) ? 1u : 0u);
           ptx::mma_commit(bar(L::bPDone));
           ptx::mma_commit(bar(L::bQEmpty + st));
         }
