@@ -160,7 +160,7 @@ FA_API fa_status fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
 
 /*
  * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs: two
- * fp32 per query row (the row's logsumexp in base-2 units and
+ * fp32 per query row (scratch derived from the row's logsumexp and from
  * D = rowsum(dout .* o)), each head's N rows rounded up to a multiple of
  * 128: 8 * B * H * ceil(N / 128) * 128 bytes.  0 for an empty problem.
  */
