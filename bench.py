@@ -29,6 +29,7 @@ import math
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -127,9 +128,7 @@ class ClockSampler:
         self.path = None
 
     def __enter__(self):
-        out_dir = os.path.join(ROOT, "gpurun_out")
-        os.makedirs(out_dir, exist_ok=True)
-        self.path = os.path.join(out_dir, "clocks_%d.csv" % os.getpid())
+        self.path = os.path.join(tempfile.gettempdir(), "fa_clocks_%d.csv" % os.getpid())
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(

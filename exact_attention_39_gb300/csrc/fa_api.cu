@@ -35,8 +35,8 @@ void *kernel_ptr() {
   return reinterpret_cast<void *>(&fa_fwd_kernel<D, T>);
 }
 
-// One-time, per-process and per-device set-up: the driver's tensor-map
-// encoder, the kernels' shared-memory opt-in, the status word's address.
+// One-time, per-process and per-device set-up: the CUDA driver's
+// tensor-map encoder, the kernels' shared-memory opt-in, the status word's address.
 fa_status ensure_ready(int dev) {
   std::lock_guard<std::mutex> lock(g_mutex);
   if (!g_encode) {
