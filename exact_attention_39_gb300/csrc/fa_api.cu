@@ -328,11 +328,12 @@ fa_status fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
   cudaStream_t up = ps[0], comp = ps[1], down = ps[2];
   cudaStream_t caller = reinterpret_cast<cudaStream_t>(stream);
 
-  // chunks of whole (batch, head) problems: up to 8, each at least one
-  const long long chunks = bh < 8 ? bh : 8;
+  // chunks of whole (batch, head) problems: up to 16, each at least one
+  constexpr int kMaxChunks = 16;
+  const long long chunks = bh < kMaxChunks ? bh : kMaxChunks;
   const size_t row_bytes = (size_t)d * 2u;
   const size_t head_bytes = (size_t)N * row_bytes, head_lse = (size_t)N * sizeof(float);
-  cudaEvent_t start, ev_in[8], ev_out[8], done;
+  cudaEvent_t start, ev_in[kMaxChunks], ev_out[kMaxChunks], done;
   if (cudaEventCreateWithFlags(&start, cudaEventDisableTiming) != cudaSuccess) return FA_ERR_CUDA;
   if (cudaEventCreateWithFlags(&done, cudaEventDisableTiming) != cudaSuccess) return FA_ERR_CUDA;
   for (int c = 0; c < chunks; ++c)
