@@ -30,10 +30,17 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 bool g_dev_ready[kMaxDevices] = {};
 unsigned *g_status_ptr[kMaxDevices] = {};
 
-template <int D, int T>
+template <int D, int T, int Q = 2>
 void *kernel_ptr() {
-  return reinterpret_cast<void *>(&fa_fwd_kernel<D, T>);
+  return reinterpret_cast<void *>(&fa_fwd_kernel<D, T, Q>);
 }
+
+// Key lengths up to which D = 64 runs one query tile per CTA, two CTAs per
+// SM (CtaShape<1>): with at most four key blocks per CTA, overlapping one
+// CTA's set-up and epilogue with the other's work pays (measured at
+// B8 H32 N512: +12 % bf16, +18 % fp16); from eight blocks on the two-tile
+// CTA is faster (N1024: -4 %, N2048: -11 % with one tile).
+constexpr int kOneTileMaxNk = 512;
 
 // One-time, per-process and per-device set-up: the CUDA driver's
 // tensor-map encoder, the kernels' shared-memory opt-in, the status word's address.
@@ -55,16 +62,26 @@ fa_status ensure_ready(int dev) {
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return FA_ERR_CUDA;
   if (major != 10 || minor != 3) return FA_ERR_CUDA;   // built for sm_103a only
-  const void *kernels[6] = {kernel_ptr<64, kF16>(), kernel_ptr<64, kBF16>(),
+  const void *kernels[9] = {kernel_ptr<64, kF16>(), kernel_ptr<64, kBF16>(),
                             kernel_ptr<64, kE4M3>(), kernel_ptr<128, kF16>(),
-                            kernel_ptr<128, kBF16>(), kernel_ptr<128, kE4M3>()};
-  const int smem[6] = {Layout<64, kF16>::kAlloc, Layout<64, kBF16>::kAlloc,
+                            kernel_ptr<128, kBF16>(), kernel_ptr<128, kE4M3>(),
+                            kernel_ptr<64, kF16, 1>(), kernel_ptr<64, kBF16, 1>(),
+                            kernel_ptr<64, kE4M3, 1>()};
+  const int smem[9] = {Layout<64, kF16>::kAlloc, Layout<64, kBF16>::kAlloc,
                        Layout<64, kE4M3>::kAlloc, Layout<128, kF16>::kAlloc,
-                       Layout<128, kBF16>::kAlloc, Layout<128, kE4M3>::kAlloc};
-  for (int t = 0; t < 6; ++t)
+                       Layout<128, kBF16>::kAlloc, Layout<128, kE4M3>::kAlloc,
+                       Layout<64, kF16, 1>::kAlloc, Layout<64, kBF16, 1>::kAlloc,
+                       Layout<64, kE4M3, 1>::kAlloc};
+  for (int t = 0; t < 9; ++t) {
     if (cudaFuncSetAttribute(kernels[t], cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem[t]) != cudaSuccess)
       return FA_ERR_CUDA;
+    // the one-tile shape needs room for two CTAs' shared memory per SM
+    if (t >= 6 && cudaFuncSetAttribute(kernels[t],
+                                       cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       100) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
   const void *bwd_kernels[8] = {
       reinterpret_cast<void *>(&fa_bwd_dq_kernel<64, kF16>),
       reinterpret_cast<void *>(&fa_bwd_dq_kernel<64, kBF16>),
@@ -116,6 +133,22 @@ bool encode_map(CUtensorMap *map, const void *base, int rows, long long bh) {
 // Encodes the maps and launches one forward kernel.  With no keys the
 // kernel loads nothing from K or V; their maps are built over q only to be
 // well formed.
+template <int D, int T, int Q>
+fa_status run_shape(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                    FwdParams p, long long bh, cudaStream_t stream) {
+  const long long units = ((long long)p.Nq + Q * kBM - 1) / (Q * kBM);
+  if (bh * units > (1ll << 31) - 1) return FA_ERR_SHAPE;
+  p.n_units = (int)units;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(bh * units), 1, 1);
+  cfg.blockDim = dim3(CtaShape<Q>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Layout<D, T, Q>::kAlloc;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, T, Q>, mq, mk, mv, p) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
 template <int D, int T>
 fa_status run(const void *q, const void *k, const void *v, FwdParams p,
               long long bh, cudaStream_t stream) {
@@ -125,14 +158,9 @@ fa_status run(const void *q, const void *k, const void *v, FwdParams p,
   if (!encode_map<D, T>(&mq, q, p.Nq, bh) || !encode_map<D, T>(&mk, kb, nk_map, bh) ||
       !encode_map<D, T>(&mv, vb, nk_map, bh))
     return FA_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(bh * p.n_units), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Layout<D, T>::kAlloc;
-  cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, T>, mq, mk, mv, p) == cudaSuccess
-             ? FA_OK
-             : FA_ERR_CUDA;
+  if constexpr (D == 64)
+    if (p.Nk <= kOneTileMaxNk) return run_shape<D, T, 1>(mq, mk, mv, p, bh, stream);
+  return run_shape<D, T, 2>(mq, mk, mv, p, bh, stream);
 }
 
 bool aligned(const void *p, uintptr_t a);

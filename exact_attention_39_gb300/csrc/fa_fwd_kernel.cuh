@@ -51,17 +51,32 @@ namespace fa {
 
 constexpr int kBM = 128;                 // query rows per tile
 constexpr int kBN = 128;                 // keys per block
-constexpr int kNumQ = 2;                 // query tiles per CTA
+constexpr int kTmemCols = 512;           // TMEM columns of an SM
+
+// Shape of a CTA with Q query tiles (Q softmax warpgroups and one control
+// warpgroup).  Q = 2 is the default: one CTA per SM.  Q = 1 (D = 64, short
+// query lengths) halves shared memory and TMEM so that two CTAs share an SM
+// and one CTA's set-up and epilogue overlap the other's work.
+template <int Q>
+struct CtaShape {
+  static constexpr int kThreads = 128 * Q + 128;
+  static constexpr int kLoadWarp = 4 * Q;
+  static constexpr int kMmaWarp = 4 * Q + 1;   // the warpgroup's last two warps idle
+  static constexpr int kMinBlocks = Q == 1 ? 2 : 1;
+  // Register split (setmaxnreg): the control warpgroup gives registers to
+  // the softmax warpgroups within the launch's budget, 65536 / kMinBlocks
+  // per CTA: Q = 2: 128*88 + 256*208 = 64512 <= 384*168; Q = 1:
+  // 128*56 + 128*200 = 32768 = 256*128.
+  static constexpr uint32_t kRegsControl = Q == 2 ? 88 : 56;
+  static constexpr uint32_t kRegsSoftmax = Q == 2 ? 208 : 200;
+  static_assert(Q == 1 || Q == 2, "one or two query tiles per CTA");
+  static_assert(128 * kRegsControl + 128 * Q * kRegsSoftmax <=
+                (uint32_t)(65536 / kMinBlocks / kThreads) / 8u * 8u * kThreads,
+                "register split exceeds the launch budget");
+};
+// Compatibility names for the default shape.
+constexpr int kNumQ = 2;
 constexpr int kRowsPerCta = kBM * kNumQ;
-constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 384;            // three warpgroups; warps 10-11 idle
-// Register split: launched at 168 per thread (65536 / 384, rounded down to
-// a multiple of 8); the producer/MMA warpgroup gives registers back to the
-// two softmax warpgroups.  128*88 + 256*208 = 64512 <= 384*168 = 64512.
-constexpr uint32_t kRegsControl = 88;
-constexpr uint32_t kRegsSoftmax = 208;
-constexpr int kTmemCols = 512;
 // A rescale of O is skipped while the running maximum grows by at most this
 // much (log2 units): probabilities then stay below 2^8, which fp16, bf16 and
 // the fp32 accumulators hold exactly as well as values below 1.
@@ -104,7 +119,7 @@ template <> struct Elem<kE4M3> {
   static constexpr bool kF8 = true;
 };
 
-template <int D, int T>
+template <int D, int T, int Q = 2>
 struct Layout {
   using E = Elem<T>;
   // Tiles are stored as chunks of kBM rows x kSwz bytes in the TMA swizzle of
@@ -117,9 +132,10 @@ struct Layout {
   static constexpr int kTileBytes = kChunks * kChunkBytes;
   static constexpr int kSBO = 8 * kSwz;                 // 8-row swizzle atom
   static constexpr uint64_t kSwzMode = kSwz == 128 ? 2 : 4;   // descriptor code
-  static constexpr int kStages = kTileBytes <= 16384 ? 4 : 2;
+  // Q = 1 keeps two stages so that two CTAs fit the SM's shared memory
+  static constexpr int kStages = Q == 1 ? 2 : (kTileBytes <= 16384 ? 4 : 2);
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kNumQ * kTileBytes;
+  static constexpr int kK = kQ + Q * kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
   static constexpr int kBars = kV + kStages * kTileBytes;
   // barrier indices
@@ -128,10 +144,10 @@ struct Layout {
   static constexpr int bVFull = bKFull + kStages;
   static constexpr int bKVEmpty = bVFull + kStages;
   static constexpr int bSFull = bKVEmpty + kStages;   // S_i ready (MMA commit)
-  static constexpr int bSFree = bSFull + kNumQ;       // S_i read into registers
-  static constexpr int bPFull = bSFree + kNumQ;       // P_i written, O_i rescaled
-  static constexpr int bODone = bPFull + kNumQ;       // O_i += P_i V_j done (commit)
-  static constexpr int bDrain = bODone + kNumQ;
+  static constexpr int bSFree = bSFull + Q;          // S_i read into registers
+  static constexpr int bPFull = bSFree + Q;           // P_i written, O_i rescaled
+  static constexpr int bODone = bPFull + Q;           // O_i += P_i V_j done (commit)
+  static constexpr int bDrain = bODone + Q;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kMisc = kBars + kNumBars * 8;   // tmem base, abort flag
   static constexpr int kBytes = kMisc + 16;
@@ -141,18 +157,20 @@ struct Layout {
   // When P fits beside the accumulators it has TMEM columns of its own, so
   // the MMA for the next block's scores may overwrite S_i as soon as softmax
   // has read it.
-  static constexpr bool kEarlyS = 256 + 2 * D + 2 * kPCols <= kTmemCols;
+  // TMEM columns the CTA allocates (a power of two, at least 32)
+  static constexpr int kTmem = Q == 2 ? kTmemCols : kTmemCols / 2;
+  static constexpr bool kEarlyS = Q * (kBN + D + kPCols) <= kTmem;
   // With the early scores the MMA thread keeps its per-block waits to three:
   // K and V of a stage land on one barrier, and one barrier each counts both
   // warpgroups' "scores read" and "P written" arrivals.  (The thread shares
   // its sub-partition with two softmax warps, so each wait it makes costs
   // issue slots that delay every later MMA.)
   static constexpr bool kMerged = kEarlyS;
-  // TMEM columns
-  __host__ __device__ static constexpr uint32_t tS(int i) { return i * 128; }
-  __host__ __device__ static constexpr uint32_t tO(int i) { return 256 + i * D; }
+  // TMEM columns: S_i, then O_i, then (early scores) P_i
+  __host__ __device__ static constexpr uint32_t tS(int i) { return i * kBN; }
+  __host__ __device__ static constexpr uint32_t tO(int i) { return Q * kBN + i * D; }
   __host__ __device__ static constexpr uint32_t tP(int i) {
-    return kEarlyS ? 256 + 2 * D + i * kPCols : i * 128;
+    return kEarlyS ? Q * (kBN + D) + i * kPCols : i * kBN;
   }
 };
 
@@ -229,13 +247,18 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity,
   }
 }
 
-template <int D, int T>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int T, int Q>
+__global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV,
                   const FwdParams p) {
-  using L = Layout<D, T>;
+  using L = Layout<D, T, Q>;
+  using C = CtaShape<Q>;
+  constexpr int kNumQ = Q;
+  constexpr int kRowsPerCta = Q * kBM;
+  constexpr int kLoadWarp = C::kLoadWarp;
+  constexpr int kMmaWarp = C::kMmaWarp;
   using E = Elem<T>;
   constexpr bool kF8 = E::kF8;
   constexpr bool kOutBF16 = T != kF16;   // e4m3 inputs give a bf16 output
@@ -262,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- set-up: TMEM, barriers
   if (warp == kMmaWarp) {
-    ptx::tmem_alloc(sbase + L::kMisc, kTmemCols);
+    ptx::tmem_alloc(sbase + L::kMisc, L::kTmem);
     ptx::tmem_relinquish();
   }
   if (threadIdx.x == 0) {
@@ -293,8 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp >= 8) {
-   ptx::regs_dec<kRegsControl>();
+  if (warp >= 4 * Q) {
+   ptx::regs_dec<C::kRegsControl>();
    // The producer and MMA warps run their loops with all 32 lanes, so every
    // operand is warp-uniform; one elected lane issues each copy, MMA and
    // commit (a commit tracks the MMAs of the lane that issues it).
@@ -459,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
    }
   } else {
     // ================================================= softmax warpgroups
-    ptx::regs_inc<kRegsSoftmax>();
+    ptx::regs_inc<C::kRegsSoftmax>();
     const int i = warp >> 2;                  // query tile of this warpgroup
     const int r = threadIdx.x & 127;          // row within the tile = TMEM lane
     const int row = q0 + i * kBM + r;         // query row within the head
@@ -628,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == kMmaWarp) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, kTmemCols);
+    ptx::tmem_dealloc(tmem, L::kTmem);
   }
 }
 
