@@ -57,7 +57,7 @@ DEFAULT_WORKLOAD = W.N8192.name
 # workload; reported only while the sources are unchanged (see
 # profiles/fa_fwd_kernel_b8h32n8192d64_bf16_launches.md).
 MEASURED_TRAFFIC = {
-    ("80170bfc1abf332c", "b8h32n8192d64_bf16"): 805.66e6 + 253.63e6,
+    ("2e47b007cdb4836e", "b8h32n8192d64_bf16"): 805.49e6 + 253.82e6,
 }
 CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw",
                 "clocks_event_reasons.active",
