@@ -506,7 +506,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto bar = [&](int idx) -> uint32_t { return bars + 8u * (uint32_t)idx; };
   volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(sm.smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm.smem + L::kMisc + 4);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
 
   const int bh = blockIdx.x / p.n_kblk;
   const int kb = blockIdx.x % p.n_kblk;      // causal: small kb has the most work
