@@ -138,3 +138,29 @@ def test_python_wrapper_validation():
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         b.load_library(str(tmp_path / "libfa_missing.so"))
+
+
+def _declared_arities():
+    """Parameter count of every function include/*.h declares."""
+    out = {}
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", fn)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"FA_API\s+[\w\s\*]+?\b(fa_\w+)\s*\(([^)]*)\)\s*;", src):
+            params = m.group(2).strip()
+            out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argument_lists_match_the_header():
+    # every ctypes prototype the binding sets up has the header's arity
+    lib = fa.load_library()
+    arities = _declared_arities()
+    assert arities, "no declarations found"
+    for name, n in arities.items():
+        fn = getattr(lib, name)
+        if fn.argtypes is not None:
+            assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
+    assert arities["fa_fwd"] == 13 and arities["fa_fwd_host"] == 18
