@@ -111,7 +111,9 @@ def test_sequence_sweep(n, causal):
 
 
 # ------------------------------------------------------------ ragged and small
-@pytest.mark.parametrize("n", [1, 2, 3, 64, 127, 128, 129, 255, 256, 257, 300, 640, 1000])
+# 511..513 straddle the switch between one and two query tiles per CTA
+@pytest.mark.parametrize("n", [1, 2, 3, 64, 127, 128, 129, 255, 256, 257, 300, 511, 512, 513,
+                               640, 1000])
 @pytest.mark.parametrize("causal", [False, True])
 def test_ragged_lengths_d64(n, causal):
     for dtype in ("fp16", "bf16"):
