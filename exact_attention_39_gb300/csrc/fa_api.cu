@@ -372,8 +372,19 @@ fa_status fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
             cudaStreamWaitEvent(up, start, 0) == cudaSuccess &&
             cudaStreamWaitEvent(comp, start, 0) == cudaSuccess &&
             cudaStreamWaitEvent(down, start, 0) == cudaSuccess;
+  // The first chunk's upload (pipeline fill) and the last chunk's kernel and
+  // download (drain) are not overlapped: those two chunks take bh / 32 heads
+  // each, the others split the rest evenly.
+  const long long edge = chunks >= 4 ? (bh / 32 > 0 ? bh / 32 : 1) : 0;
+  auto bound = [&](long long c) -> long long {   // first head of chunk c
+    if (edge == 0) return bh * c / chunks;
+    if (c == 0) return 0;
+    if (c == chunks) return bh;
+    if (c == chunks - 1) return bh - edge;
+    return edge + (bh - 2 * edge) * (c - 1) / (chunks - 2);
+  };
   for (long long c = 0; ok && c < chunks; ++c) {
-    const long long h0 = bh * c / chunks, h1 = bh * (c + 1) / chunks, nh = h1 - h0;
+    const long long h0 = bound(c), h1 = bound(c + 1), nh = h1 - h0;
     const size_t off = (size_t)h0 * head_bytes, bytes = (size_t)nh * head_bytes;
     const size_t loff = (size_t)h0 * head_lse, lbytes = (size_t)nh * head_lse;
     char *qd = static_cast<char *>(q_d) + off, *kd = static_cast<char *>(k_d) + off;
