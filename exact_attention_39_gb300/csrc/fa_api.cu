@@ -173,13 +173,37 @@ cudaStream_t g_pipe[kMaxDevices][kPipeStreams] = {};
 fa_status pipe_streams(int dev, cudaStream_t **out) {
   std::lock_guard<std::mutex> lock(g_mutex);
   if (!g_pipe[dev][0]) {
+    // published only once all three exist: a half-made set would leave null
+    // (legacy default) streams in the table
+    cudaStream_t made[kPipeStreams] = {};
     for (int t = 0; t < kPipeStreams; ++t)
-      if (cudaStreamCreateWithFlags(&g_pipe[dev][t], cudaStreamNonBlocking) != cudaSuccess)
+      if (cudaStreamCreateWithFlags(&made[t], cudaStreamNonBlocking) != cudaSuccess) {
+        for (int u = 0; u < t; ++u) cudaStreamDestroy(made[u]);
         return FA_ERR_CUDA;
+      }
+    for (int t = 0; t < kPipeStreams; ++t) g_pipe[dev][t] = made[t];
   }
   *out = g_pipe[dev];
   return FA_OK;
 }
+
+// The events of one fa_fwd_host call, destroyed when the call returns (an
+// event destroyed while its record is pending is released once the record
+// completes).
+template <int N>
+struct EventSet {
+  cudaEvent_t ev[N] = {};
+  int made = 0;
+  bool create() {
+    for (; made < N; ++made)
+      if (cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming) != cudaSuccess)
+        return false;
+    return true;
+  }
+  ~EventSet() {
+    for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);
+  }
+};
 
 struct WaitTestParams {
   unsigned long long timeout_ns;
@@ -361,13 +385,10 @@ fa_status fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
   const long long chunks = bh < kMaxChunks ? bh : kMaxChunks;
   const size_t row_bytes = (size_t)d * 2u;
   const size_t head_bytes = (size_t)N * row_bytes, head_lse = (size_t)N * sizeof(float);
-  cudaEvent_t start, ev_in[kMaxChunks], ev_out[kMaxChunks], done;
-  if (cudaEventCreateWithFlags(&start, cudaEventDisableTiming) != cudaSuccess) return FA_ERR_CUDA;
-  if (cudaEventCreateWithFlags(&done, cudaEventDisableTiming) != cudaSuccess) return FA_ERR_CUDA;
-  for (int c = 0; c < chunks; ++c)
-    if (cudaEventCreateWithFlags(&ev_in[c], cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&ev_out[c], cudaEventDisableTiming) != cudaSuccess)
-      return FA_ERR_CUDA;
+  EventSet<2 * kMaxChunks + 2> events;
+  if (!events.create()) return FA_ERR_CUDA;
+  cudaEvent_t start = events.ev[0], fin = events.ev[1];
+  cudaEvent_t *ev_in = events.ev + 2, *ev_out = events.ev + 2 + kMaxChunks;
   bool ok = cudaEventRecord(start, caller) == cudaSuccess &&
             cudaStreamWaitEvent(up, start, 0) == cudaSuccess &&
             cudaStreamWaitEvent(comp, start, 0) == cudaSuccess &&
@@ -409,16 +430,14 @@ fa_status fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
          cudaMemcpyAsync(reinterpret_cast<char *>(lse_h) + loff, ld, lbytes,
                          cudaMemcpyDeviceToHost, down) == cudaSuccess;
   }
-  if (ok)
-    ok = cudaEventRecord(done, down) == cudaSuccess &&
-         cudaStreamWaitEvent(caller, done, 0) == cudaSuccess;
-  // events are released once the work they mark has completed
-  cudaEventDestroy(start);
-  cudaEventDestroy(done);
-  for (int c = 0; c < chunks; ++c) {
-    cudaEventDestroy(ev_in[c]);
-    cudaEventDestroy(ev_out[c]);
-  }
+  // `stream` waits for all three streams, also after a failure part way, so
+  // that work the caller orders after this call never overtakes a copy this
+  // call enqueued (on success the downloads come last and the other two
+  // waits are already satisfied).
+  for (cudaStream_t ps_t : {up, comp, down})
+    if (cudaEventRecord(fin, ps_t) != cudaSuccess ||
+        cudaStreamWaitEvent(caller, fin, 0) != cudaSuccess)
+      ok = false;
   if (!ok) return st != FA_OK ? st : FA_ERR_CUDA;
   return FA_OK;
 }
