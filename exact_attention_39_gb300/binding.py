@@ -97,6 +97,19 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _require_on(device, what, *tensors):
+    """Every tensor a contiguous CUDA tensor on ``device``: the library runs on
+    the current device and dereferences every pointer there."""
+    for t in tensors:
+        if not t.is_cuda or t.device != device or not t.is_contiguous():
+            raise ValueError("%s must be contiguous CUDA tensors on %s" % (what, device))
+
+
+def _require_stream_on(device, stream):
+    if stream is not None and stream.device != device:
+        raise ValueError("stream is on %s, the tensors on %s" % (stream.device, device))
+
+
 def fa_fwd_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, causal,
                scale, dtype_code, stream_handle):
     """The C call with plain integers; returns the status code."""
@@ -149,9 +162,10 @@ def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None):
     if not (q.dtype == k.dtype == v.dtype):
         raise TypeError("q, k, v must share one dtype")
     code = _dtype_code(q)
-    for t in (q, k, v):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    if not q.is_cuda:
+        raise ValueError("q, k, v must be contiguous CUDA tensors")
+    _require_on(q.device, "q, k, v", q, k, v)
+    _require_stream_on(q.device, stream)
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
     if scale is None:
@@ -160,10 +174,11 @@ def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, stream=None):
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+    if out.shape != q.shape or out.dtype != q.dtype:
         raise ValueError("out must be a contiguous tensor like q")
-    if lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+    if lse.shape != (B, H, Nq) or lse.dtype != torch.float32:
         raise ValueError("lse must be a contiguous float32 [B, H, Nq] tensor")
+    _require_on(q.device, "out and lse", out, lse)
     with torch.cuda.device(q.device):
         if Nq == Nk:
             st = fa_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(),
@@ -188,8 +203,10 @@ def fwd_fp8(q, k, v, q_descale, k_descale, v_descale, causal=False,
     for t in (q, k, v):
         if t.dtype != torch.float8_e4m3fn:
             raise TypeError("q, k, v must be torch.float8_e4m3fn")
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("q, k, v must be contiguous CUDA tensors")
+    if not q.is_cuda:
+        raise ValueError("q, k, v must be contiguous CUDA tensors")
+    _require_on(q.device, "q, k, v", q, k, v)
+    _require_stream_on(q.device, stream)
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
     if scale is None:
@@ -198,10 +215,11 @@ def fwd_fp8(q, k, v, q_descale, k_descale, v_descale, causal=False,
         out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    if out.shape != (B, H, Nq, d) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+    if out.shape != (B, H, Nq, d) or out.dtype != torch.bfloat16:
         raise ValueError("out must be a contiguous bf16 [B, H, Nq, d] tensor")
-    if lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+    if lse.shape != (B, H, Nq) or lse.dtype != torch.float32:
         raise ValueError("lse must be a contiguous float32 [B, H, Nq] tensor")
+    _require_on(q.device, "out and lse", out, lse)
     with torch.cuda.device(q.device):
         _check(fa_fwd_fp8_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                               out.data_ptr(), lse.data_ptr(), B, H, Nq, Nk, d,
@@ -250,9 +268,10 @@ def bwd(q, k, v, o, lse, dout, causal=False, scale=None, dq=None, dk=None,
     if not (q.dtype == k.dtype == v.dtype == o.dtype == dout.dtype):
         raise TypeError("q, k, v, o, dout must share one dtype")
     code = _dtype_code(q)
-    for t in (q, k, v, o, dout, lse):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("inputs must be contiguous CUDA tensors")
+    if not q.is_cuda:
+        raise ValueError("inputs must be contiguous CUDA tensors")
+    _require_on(q.device, "inputs", q, k, v, o, dout, lse)
+    _require_stream_on(q.device, stream)
     B, H, N, d = q.shape
     if lse.shape != (B, H, N) or lse.dtype != torch.float32:
         raise ValueError("lse must be a float32 [B, H, N] tensor")
@@ -262,11 +281,13 @@ def bwd(q, k, v, o, lse, dout, causal=False, scale=None, dq=None, dk=None,
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     for t in (dq, dk, dv):
-        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+        if t.shape != q.shape or t.dtype != q.dtype:
             raise ValueError("dq, dk, dv must be contiguous tensors like q")
+    _require_on(q.device, "dq, dk, dv", dq, dk, dv)
     need = bwd_workspace_bytes(B, H, N)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _require_on(q.device, "workspace", workspace)
     with torch.cuda.device(q.device):
         _check(fa_bwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                           dout.data_ptr(), lse.data_ptr(), dq.data_ptr(),
@@ -295,9 +316,10 @@ def fwd_host(q_h, k_h, v_h, q_d, k_d, v_d, o_d, lse_d, o_h, lse_h,
     for t in (q_h, k_h, v_h, o_h, lse_h):
         if t.device.type != "cpu" or not t.is_contiguous():
             raise ValueError("host tensors must be contiguous CPU tensors")
-    for t in (q_d, k_d, v_d, o_d, lse_d):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("staging tensors must be contiguous CUDA tensors")
+    if not q_d.is_cuda:
+        raise ValueError("staging tensors must be contiguous CUDA tensors")
+    _require_on(q_d.device, "staging tensors", q_d, k_d, v_d, o_d, lse_d)
+    _require_stream_on(q_d.device, stream)
     if q_h.dim() != 4 or k_h.shape != q_h.shape or v_h.shape != q_h.shape:
         raise ValueError("q, k, v must share one [B, H, N, d] shape")
     for a, b in ((q_h, q_d), (k_h, k_d), (v_h, v_d), (o_h, o_d), (lse_h, lse_d)):
@@ -309,12 +331,13 @@ def fwd_host(q_h, k_h, v_h, q_d, k_d, v_d, o_d, lse_d, o_h, lse_h,
     if lse_h.shape != (B, H, N) or lse_h.dtype != torch.float32:
         raise ValueError("lse must be float32 [B, H, N]")
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    stream = stream or torch.cuda.current_stream()
-    _check(fa_fwd_host_raw(q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(),
-                           o_h.data_ptr(), lse_h.data_ptr(), q_d.data_ptr(),
-                           k_d.data_ptr(), v_d.data_ptr(), o_d.data_ptr(),
-                           lse_d.data_ptr(), B, H, N, d, causal, scale,
-                           _dtype_code(q_h), _stream_handle(stream)))
+    with torch.cuda.device(q_d.device):
+        stream = stream or torch.cuda.current_stream()
+        _check(fa_fwd_host_raw(q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(),
+                               o_h.data_ptr(), lse_h.data_ptr(), q_d.data_ptr(),
+                               k_d.data_ptr(), v_d.data_ptr(), o_d.data_ptr(),
+                               lse_d.data_ptr(), B, H, N, d, causal, scale,
+                               _dtype_code(q_h), _stream_handle(stream)))
     stream.synchronize()
     return o_h, lse_h
 

@@ -254,6 +254,39 @@ def test_host_buffers_match_device_call(B, H, N, causal, dtype):
     assert fa.last_device_error() == 0
 
 
+def test_wrappers_reject_buffers_off_the_device():
+    # Every pointer the library receives is dereferenced on the current
+    # device, so the wrappers refuse host or non-contiguous tensors before
+    # anything is enqueued.
+    w = W.Workload("dev", 1, 2, 128, 64, "bf16", False, seed=3)
+    q, k, v = (t.cuda() for t in W.make_inputs(w))
+    lse = torch.empty(1, 2, 128, dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError):
+        fa.fwd(q, k, v, out=torch.empty_like(q, device="cpu"))
+    with pytest.raises(ValueError):
+        fa.fwd(q, k, v, lse=lse.cpu())
+    with pytest.raises(ValueError):
+        fa.fwd(q, k, v, out=torch.empty(1, 2, 64, 128, dtype=q.dtype,
+                                        device="cuda").transpose(2, 3))
+    with pytest.raises(ValueError):
+        fa.fwd(q, k.cpu(), v)
+    o, lse = fa.fwd(q, k, v)
+    with pytest.raises(ValueError):
+        fa.bwd(q, k, v, o, lse, o, workspace=torch.empty(1 << 12, dtype=torch.uint8))
+    with pytest.raises(ValueError):
+        fa.bwd(q, k, v, o, lse, o, dq=torch.empty_like(q, device="cpu"))
+    q8 = q.to(torch.float8_e4m3fn)
+    with pytest.raises(ValueError):
+        fa.fwd_fp8(q8, q8, q8, 1.0, 1.0, 1.0, lse=lse.cpu())
+    host = [t.cpu().pin_memory() for t in (q, k, v)]
+    oh = torch.empty_like(host[0]).pin_memory()
+    lh = torch.empty(1, 2, 128, dtype=torch.float32).pin_memory()
+    with pytest.raises(ValueError):
+        fa.fwd_host(*host, q, k, v.cpu(), o, lse, oh, lh)
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
+
+
 def test_outputs_do_not_touch_neighbours():
     # O and LSE are written only inside their [B, H, N, d] / [B, H, N] spans.
     w = W.Workload("guard", 1, 2, 300, 64, "bf16", True, seed=8)
