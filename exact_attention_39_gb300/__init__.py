@@ -9,6 +9,7 @@ from .binding import (FaError, bwd, bwd_workspace_bytes, fwd,  # noqa: F401
                       fwd_fp8, fwd_host, last_device_error, load_library,
                       status_string, version)
 from . import workloads  # noqa: F401
+from .shard import fwd_shard, head_range  # noqa: F401
 
 __all__ = ["fwd", "fwd_fp8", "fwd_host", "bwd", "bwd_workspace_bytes", "last_device_error", "load_library",
-           "status_string", "version", "FaError", "workloads"]
+           "status_string", "version", "FaError", "workloads", "fwd_shard", "head_range"]
