@@ -100,6 +100,7 @@ typedef struct {
     long nrows;
     double *o, *lse;
     long next;        /* next work item, shared */
+    int running;      /* workers that got their scratch and take items */
     pthread_mutex_t lock;
 } oracle_job;
 
@@ -107,7 +108,10 @@ static void *worker(void *arg)
 {
     oracle_job *jb = (oracle_job *)arg;
     double *w = (double *)malloc(sizeof(double) * (size_t)(jb->Nk > 0 ? jb->Nk : 1));
-    if (!w) return NULL;
+    if (!w) return NULL;   /* takes no items; another worker does them */
+    pthread_mutex_lock(&jb->lock);
+    jb->running += 1;
+    pthread_mutex_unlock(&jb->lock);
     const long total = jb->BH * jb->nrows;
     const long chunk = 16;
     for (;;) {
@@ -139,7 +143,8 @@ static void *worker(void *arg)
  *         (the same subset for every head).
  *   o: [BH, nrows, d]; lse: [BH, nrows]   (nrows = Nq when rows is NULL)
  *   nthreads <= 0 uses one thread.
- * Returns 0 on success, -1 on bad arguments.
+ * Returns 0 on success, -1 on bad arguments or when no worker could
+ * allocate its scratch (then nothing was computed).
  */
 int fa_oracle_fwd(const double *q, const double *k, const double *v,
                   long BH, long Nq, long Nk, long d, int causal, double scale,
@@ -163,6 +168,7 @@ int fa_oracle_fwd(const double *q, const double *k, const double *v,
     jb.rows = rows; jb.nrows = nrows;
     jb.o = o; jb.lse = lse;
     jb.next = 0;
+    jb.running = 0;
     pthread_mutex_init(&jb.lock, NULL);
 
     pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
@@ -174,7 +180,8 @@ int fa_oracle_fwd(const double *q, const double *k, const double *v,
     for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
     free(tid);
     pthread_mutex_destroy(&jb.lock);
-    return 0;
+    /* any worker that started keeps taking items until none are left */
+    return jb.running > 0 ? 0 : -1;
 }
 
 /*
@@ -199,6 +206,7 @@ typedef struct {
     long row0, row1;
     double *dq;               /* rows row0..row1 of dQ for this head */
     double *dk, *dv;          /* chunk-private [Nk, d] partial sums  */
+    int failed;               /* set when the chunk could not run    */
 } bwd_chunk;
 
 static void *bwd_worker(void *arg)
@@ -207,7 +215,7 @@ static void *bwd_worker(void *arg)
     const long d = c->d, Nk = c->Nk;
     double *w = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
     double *o_row = (double *)malloc(sizeof(double) * (size_t)d);
-    if (!w || !o_row) { free(w); free(o_row); return NULL; }
+    if (!w || !o_row) { free(w); free(o_row); c->failed = 1; return NULL; }
     for (long i = c->row0; i < c->row1; ++i) {
         const double *qi = c->q + i * d, *gi = c->dout + i * d;
         double lse;
@@ -269,6 +277,7 @@ int fa_oracle_bwd(const double *q, const double *k, const double *v,
             c->dq = dq + (h * Nq + c->row0) * d;
             c->dk = part + (2 * t) * Nk * d;
             c->dv = part + (2 * t + 1) * Nk * d;
+            c->failed = 0;
             memset(c->dk, 0, sizeof(double) * (size_t)(2 * Nk * d));
         }
         int started = 0;
@@ -276,6 +285,9 @@ int fa_oracle_bwd(const double *q, const double *k, const double *v,
             if (pthread_create(&tid[started], NULL, bwd_worker, &ch[started]) != 0) break;
         for (long t = started; t < nchunks; ++t) bwd_worker(&ch[t]);
         for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+        int failed = 0;
+        for (long t = 0; t < nchunks; ++t) failed |= ch[t].failed;
+        if (failed) { free(ch); free(part); free(tid); return -1; }
         double *dkh = dk + h * Nk * d, *dvh = dv + h * Nk * d;
         for (long e = 0; e < Nk * d; ++e) { dkh[e] = 0.0; dvh[e] = 0.0; }
         for (long t = 0; t < nchunks; ++t)
