@@ -150,7 +150,10 @@ FA_API fa_status fa_fwd_fp8(const void *q, const void *k, const void *v,
  * after the work already enqueued on `stream`, and `stream` waits for the
  * last download, so synchronising `stream` makes o_h and lse_h valid.
  * Errors as fa_fwd (checked before anything is enqueued), plus FA_ERR_NULL
- * for a missing host or staging buffer.
+ * for a missing host or staging buffer.  A CUDA call that fails part way
+ * returns FA_ERR_CUDA; `stream` still waits for every copy and kernel
+ * enqueued before the failure, so after synchronising it no copy touches
+ * the buffers any more (their contents are then unspecified).
  */
 FA_API fa_status fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
                              void *o_h, float *lse_h, void *q_d, void *k_d,
