@@ -89,3 +89,40 @@ def test_reference_cli_prints_one_contract_line():
     assert d["config"]["workload"] == "b8h32n512d64_bf16"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_clock_summary_reads_reasons_and_loaded_clock(tmp_path):
+    # nvidia-smi rows as the sampler writes them (csv, noheader, nounits):
+    # index, sm MHz, max sm MHz, power W, active mask, then four reasons
+    rows = ["0, 1980, 2070, 120.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "0, 2055, 2070, 900.0, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 2040, 2070, 950.0, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 2070, 2070, 980.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "garbage line"]
+    path = tmp_path / "clocks.csv"
+    path.write_text("\n".join(rows) + "\n")
+    s = bench.ClockSampler(0)
+    s.proc, s.path = object(), str(path)
+    out = s.summary()
+    assert out["reasons"] == ["sw_power_cap"]
+    assert out["sm_max_mhz"] == 2070.0 and out["samples"] == 4
+    # median over the samples drawing at least half the peak power (the idle
+    # 120 W sample is left out)
+    assert out["sm_mhz"] == 2055.0 and out["power_w_max"] == 980.0
+    assert not path.exists()          # the sampler's file is removed once read
+
+
+def test_clock_summary_flags_throttling_and_missing_samples(tmp_path):
+    path = tmp_path / "clocks.csv"
+    path.write_text("0, 1500, 2070, 800.0, 0x8, Active, Not Active, Active, Not Active\n")
+    s = bench.ClockSampler(0)
+    s.proc, s.path = object(), str(path)
+    assert s.summary()["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+    empty = bench.ClockSampler(0)
+    assert empty.summary()["reasons"] == ["unsampled"]
+
+
+def test_l2_note_names_the_flush_rule():
+    assert "no flush" in bench.l2_note(bench.WORKLOADS["b8h32n8192d64_bf16"])
+    assert "> 129 MB L2" in bench.l2_note(bench.WORKLOADS["b8h32n8192d64_bf16"])
+    assert "fit in the 129 MB L2" in bench.l2_note(bench.WORKLOADS["b8h32n512d64_fp16"])
