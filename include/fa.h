@@ -182,7 +182,12 @@ FA_API size_t fa_bwd_workspace_bytes(int B, int H, int N);
  *                      fa_bwd_workspace_bytes(B, H, N) bytes, 16-byte
  *                      aligned; its contents on entry do not matter, and
  *                      calls that run concurrently need separate workspaces.
- * P is recomputed from q, k and lse, never stored.  Three kernels are
+ * P is recomputed from q, k and lse, never stored: the attention matrix
+ * costs no memory in the backward either ("0 MB (recompute)" in the Flash
+ * Attention 2 memory table, baguaai.com/zh/skills/benchmarks-332e54,
+ * "内存使用分析"; the same page lists training performance, i.e. forward
+ * and backward, among its benchmarks).  The gradient formulas are the
+ * chain rule through softmax(scale Q K^T) V.  Three kernels are
  * enqueued on `stream` (row sums, dQ, then dK and dV).  Errors as fa_fwd,
  * plus FA_ERR_WORKSPACE.  d is 64 or 128; dtype FA_FP16 or FA_BF16.
  */
