@@ -468,7 +468,7 @@ def run_gpu(args, w, world, rank, local):
                                        if sm_mhz else None),
                 "hbm_gbs_algorithmic": w.hbm_bytes() / (kern_avg_ms * 1e-3) / 1e9}
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:   # the CPU leg runs at N = 1 only
         secs, fl, heads, nt, one = time_oracle(w, args.cpu_budget, args.cpu_max_heads)
         cpu = {"value": fl / secs / 1e12, "unit": UNIT, "cores": nt,
                "kind": "oracle",
