@@ -1,7 +1,7 @@
 """Pins for the fp64 backward oracle (no GPU).
 
 The gradients of L = sum(O * dO) are pinned to what the mathematics fixes:
-central finite differences of the (separately pinned) forward oracle along
+hand-derived worked examples, central finite differences of the (separately pinned) forward oracle along
 random directions, an unfused brute force, closed forms and invariants of
 the softmax Jacobian.
 """
@@ -19,6 +19,48 @@ def rnd(shape, seed):
 def loss(q, k, v, g, scale, causal):
     o, _ = oracle.attention_fwd(q, k, v, scale, causal)
     return float(np.sum(o * g))
+
+
+# ---------------------------------------------------------------- worked examples
+def test_two_key_worked_example():
+    # d = 2, scale 1/2, one query q = (2a, 2 ln 3), keys k0 = (1, 0),
+    # k1 = (1, 1): logits (a, a + ln 3), so p = (1/4, 3/4).  v0 = (4, 0),
+    # v1 = (0, 8) give O = (1, 6).  Upstream g = (1, 2):
+    #   D = g.O = 13,  dP = (g.v0, g.v1) = (4, 16),
+    #   dS = p * (dP - D) = (-9/4, 9/4),
+    #   dV_j = p_j g = (1/4, 1/2), (3/4, 3/2),
+    #   dQ = scale * sum_j dS_j k_j = (0, 9/8),
+    #   dK_j = scale * dS_j q = dS_j * (a, ln 3).
+    # A dropped scale doubles dQ and dK; a flipped sign or a transposed K
+    # changes every entry.
+    a, ln3 = 0.5, np.log(3.0)
+    q = np.array([[2 * a, 2 * ln3]])
+    k = np.array([[1.0, 0.0], [1.0, 1.0]])
+    v = np.array([[4.0, 0.0], [0.0, 8.0]])
+    g = np.array([[1.0, 2.0]])
+    dq, dk, dv = oracle.attention_bwd(q, k, v, g, 0.5, False)
+    np.testing.assert_allclose(dq, [[0.0, 9 / 8]], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(dk, [[-9 / 4 * a, -9 / 4 * ln3], [9 / 4 * a, 9 / 4 * ln3]],
+                               rtol=0, atol=1e-14)
+    np.testing.assert_allclose(dv, [[0.25, 0.5], [0.75, 1.5]], rtol=0, atol=1e-14)
+
+
+def test_causal_worked_example():
+    # d = 1, scale 1, q = (1, 1), k = (0, ln 3), v = (2, 6), g = (1, 1).
+    # Row 0 sees key 0 only: p = (1, 0), O = 2, dS = 1 * (2 - 2) = 0.
+    # Row 1 sees both: p = (1/4, 3/4), O = 5, dP = (2, 6),
+    #   dS = (1/4 (2 - 5), 3/4 (6 - 5)) = (-3/4, 3/4), dQ_1 = 3/4 ln 3.
+    # Summed over rows: dV = (1 + 1/4, 3/4), dK = (-3/4, 3/4).  With the mask
+    # reversed, row 0 would see key 1 and every entry would change.
+    ln3 = np.log(3.0)
+    q = np.array([[1.0], [1.0]])
+    k = np.array([[0.0], [ln3]])
+    v = np.array([[2.0], [6.0]])
+    g = np.array([[1.0], [1.0]])
+    dq, dk, dv = oracle.attention_bwd(q, k, v, g, 1.0, True)
+    np.testing.assert_allclose(dq, [[0.0], [0.75 * ln3]], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(dk, [[-0.75], [0.75]], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(dv, [[1.25], [0.75]], rtol=0, atol=1e-14)
 
 
 @pytest.mark.parametrize("nq,nk,causal", [(24, 24, False), (24, 24, True),
