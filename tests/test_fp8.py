@@ -143,3 +143,18 @@ def test_fp8_wrapper_rejects_other_dtypes():
     q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         fa.fwd_fp8(q, q, q, 1.0, 1.0, 1.0)
+
+
+def test_e4m3_rounding_bound_behind_the_tolerance():
+    # The tolerance above rests on |Q(p) - p| <= 2^-4 p + 2^-10 for e4m3
+    # round-to-nearest over the range P takes (0 .. 256, within e4m3's 448):
+    # 3 mantissa bits give half a unit of 2^-3 relative for normal values,
+    # and subnormals are spaced 2^-9 apart.  A dense sweep checks it, and that
+    # it is close to tight (a 2^-5 relative bound fails).
+    p = torch.cat([torch.linspace(0.0, 256.0, 1_000_001, dtype=torch.float64),
+                   torch.linspace(0.0, 0.02, 100_001, dtype=torch.float64)])
+    qp = p.float().to(torch.float8_e4m3fn).double()
+    err = (qp - p).abs()
+    assert bool((err <= 2.0 ** -4 * p + 2.0 ** -10).all())
+    assert bool((err > 2.0 ** -5 * p + 2.0 ** -10).any())
+    assert float(torch.tensor(256.0).to(torch.float8_e4m3fn).double()) == 256.0
