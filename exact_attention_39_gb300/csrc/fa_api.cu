@@ -111,7 +111,7 @@ fa_status ensure_ready(int dev) {
 // 128 x 1 elements in the swizzle the kernel's layout names.  Rows past
 // `rows` within a head read as zero.
 template <int D, int T>
-bool encode_map(CUtensorMap *map, const void *base, int rows, long long bh) {
+bool encode_map_uncached(CUtensorMap *map, const void *base, int rows, long long bh) {
   using L = Layout<D, T>;
   const cuuint64_t eb = (cuuint64_t)Elem<T>::kBytes;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)bh};
@@ -128,6 +128,49 @@ bool encode_map(CUtensorMap *map, const void *base, int rows, long long bh) {
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// A tensor map depends only on (base address, rows, heads, head dim, element
+// type), so the maps of recent calls are kept and reused: a call on the same
+// buffers skips the driver's encoder.  Small and round-robin; a map is a
+// plain 128-byte value (no driver object to release).
+struct MapKey {
+  const void *base;
+  long long bh;
+  int rows, d, t;
+  bool operator==(const MapKey &o) const {
+    return base == o.base && bh == o.bh && rows == o.rows && d == o.d && t == o.t;
+  }
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  bool valid;
+};
+constexpr int kMapCacheSize = 64;
+MapEntry g_map_cache[kMapCacheSize] = {};
+int g_map_next = 0;
+std::mutex g_map_mutex;
+
+template <int D, int T>
+bool encode_map(CUtensorMap *map, const void *base, int rows, long long bh) {
+  const MapKey key{base, bh, rows, D, T};
+  {
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    for (const MapEntry &e : g_map_cache)
+      if (e.valid && e.key == key) {
+        *map = e.map;
+        return true;
+      }
+  }
+  if (!encode_map_uncached<D, T>(map, base, rows, bh)) return false;
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  MapEntry &e = g_map_cache[g_map_next];
+  g_map_next = (g_map_next + 1) % kMapCacheSize;
+  e.key = key;
+  e.map = *map;
+  e.valid = true;
+  return true;
 }
 
 // Encodes the maps and launches one forward kernel.  With no keys the
@@ -457,21 +500,53 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N) {
   return 2 * (size_t)B * (size_t)H * n_pad * sizeof(float);
 }
 
+}  // extern "C"
+
+namespace fa {
+namespace {
+
+// The host-side checks of fa_bwd that need no workspace, in the order fa_bwd
+// makes them; none of them touches CUDA.  Returns FA_OK with *empty set for
+// a problem with no rows.
+fa_status bwd_host_checks(const void *q, const void *k, const void *v, const void *o,
+                          const void *dout, const float *lse, const void *dq,
+                          const void *dk, const void *dv, int B, int H, int N, int d,
+                          float scale, fa_dtype dtype, bool *empty) {
+  *empty = false;
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_DTYPE;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+  if (B == 0 || H == 0 || N == 0) {   // empty problem
+    *empty = true;
+    return FA_OK;
+  }
+  // B*H bounded before any product with it; N padded to whole 128-row blocks
+  // must stay an int
+  if ((long long)B * (long long)H > (1ll << 31) - 1) return FA_ERR_SHAPE;
+  if (((long long)N + kBM - 1) / kBM * kBM > (1ll << 31) - 1) return FA_ERR_SHAPE;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_NULL;
+  if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
+    return FA_ERR_ALIGN;
+  return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
 fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
                  const void *dout, const float *lse, void *dq, void *dk, void *dv,
                  void *workspace, size_t workspace_bytes, int B, int H, int N,
                  int d, int causal, float scale, fa_dtype dtype,
                  fa_stream_t stream) {
   using namespace fa;
-  if (B < 0 || H < 0 || N < 0) return FA_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
-  if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_DTYPE;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
-  if (B == 0 || H == 0 || N == 0) return FA_OK;   // empty problem
   // every host-side check before the first CUDA call
-  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_NULL;
-  if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
-    return FA_ERR_ALIGN;
+  bool empty = false;
+  fa_status hst = bwd_host_checks(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale,
+                                  dtype, &empty);
+  if (hst != FA_OK || empty) return hst;
   if (!workspace || !aligned(workspace, 16) ||
       workspace_bytes < fa_bwd_workspace_bytes(B, H, N))
     return FA_ERR_WORKSPACE;
@@ -485,7 +560,7 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
   p.o = o;
   p.dout = dout;
   p.lse = lse;
-  p.n_pad = (N + kBM - 1) / kBM * kBM;
+  p.n_pad = (int)(((long long)N + kBM - 1) / kBM * kBM);   // <= INT_MAX, checked
   p.nlse2 = static_cast<float *>(workspace);
   p.ndsum = p.nlse2 + (size_t)bh * (size_t)p.n_pad;
   p.dq = dq;
@@ -600,10 +675,13 @@ fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v,
                          int d, int causal, float scale, fa_dtype dtype,
                          fa_stream_t stream) {
   using namespace fa;
-  if (B < 0 || H < 0 || N < 0) return FA_ERR_SHAPE;
-  if (B == 0 || H == 0 || N == 0)   // empty problem: fa_bwd's checks, no scratch
-    return fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, nullptr, 0, B, H, N, d,
-                  causal, scale, dtype, stream);
+  // fa_bwd's host-side checks first, so that a bad argument gets fa_bwd's
+  // error and nothing touches CUDA before they pass
+  bool empty = false;
+  const fa_status hst = bwd_host_checks(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d,
+                                        scale, dtype, &empty);
+  if (hst != FA_OK || empty) return hst;
+  // B*H < 2^31 and n_pad < 2^31 (checked above): the product fits in 64 bits
   const long long n_pad = ((long long)N + kBM - 1) / kBM * kBM;
   if ((long long)B * (long long)H * n_pad > kNoAllocMaxRows) return FA_ERR_WORKSPACE;
   int dev = 0;

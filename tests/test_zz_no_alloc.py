@@ -64,3 +64,55 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     assert st == b.FA_ERR_WORKSPACE
     assert b.fa_bwd_noalloc_raw(0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 1, 1, 64, 0, 0.125,
                                 b.FA_BF16, ctypes.c_void_p(0)) == b.FA_OK
+
+
+def test_noalloc_checks_arguments_like_fa_bwd_before_any_cuda_call():
+    # A problem of exactly the scratch's capacity passes the capacity check
+    # and then meets fa_bwd's own checks, which run before anything touches
+    # CUDA (so these hold on a machine without a GPU).
+    P = 0x10000
+    s0 = ctypes.c_void_p(0)
+    cap = b.FA_BWD_NOALLOC_MAX_ROWS
+    n_at_cap = cap // 32                  # B = 1, H = 32: exactly the capacity
+    assert n_at_cap % 128 == 0
+    assert b.fa_bwd_noalloc_raw(0, 0, 0, 0, 0, 0, 0, 0, 0, 1, 32, n_at_cap, 64, 0, 0.125,
+                                b.FA_BF16, s0) == b.FA_ERR_NULL
+    # one padded block more is over the capacity
+    assert b.fa_bwd_noalloc_raw(P, P, P, P, P, P, P, P, P, 1, 32, n_at_cap + 1, 64, 0,
+                                0.125, b.FA_BF16, s0) == b.FA_ERR_WORKSPACE
+    # fa_bwd's errors, not a CUDA error, for bad arguments of an in-range shape
+    assert b.fa_bwd_noalloc_raw(P, P, P, P, P, P, P, P, P, 1, 2, 256, 96, 0, 0.125,
+                                b.FA_BF16, s0) == b.FA_ERR_HEADDIM
+    assert b.fa_bwd_noalloc_raw(P, P, P, P, P, P, P, P, P, 1, 2, 256, 64, 0, 0.125,
+                                7, s0) == b.FA_ERR_DTYPE
+    assert b.fa_bwd_noalloc_raw(P, P, P, P, P, P, P, P, P, 1, 2, 256, 64, 0, -1.0,
+                                b.FA_BF16, s0) == b.FA_ERR_SCALE
+    assert b.fa_bwd_noalloc_raw(P, P, P, P, P, P, P + 8, P, P, 1, 2, 256, 64, 0, 0.125,
+                                b.FA_BF16, s0) == b.FA_ERR_ALIGN
+
+
+def test_noalloc_and_bwd_reject_shapes_that_overflow():
+    # B * H beyond 2^31 - 1, and N whose padding to whole blocks leaves int
+    P = 0x10000
+    s0 = ctypes.c_void_p(0)
+    big = 1 << 16
+    assert b.fa_bwd_noalloc_raw(P, P, P, P, P, P, P, P, P, big, big, 1 << 30, 64, 0, 0.125,
+                                b.FA_BF16, s0) == b.FA_ERR_SHAPE
+    assert b.fa_bwd_raw(P, P, P, P, P, P, P, P, P, P, 1 << 40, big, big, 1 << 30, 64, 0,
+                        0.125, b.FA_BF16, s0) == b.FA_ERR_SHAPE
+    n_max = (1 << 31) - 1
+    assert b.fa_bwd_noalloc_raw(P, P, P, P, P, P, P, P, P, 1, 1, n_max, 64, 0, 0.125,
+                                b.FA_BF16, s0) == b.FA_ERR_SHAPE
+    assert b.fa_bwd_raw(P, P, P, P, P, P, P, P, P, P, 1 << 40, 1, 1, n_max, 64, 0, 0.125,
+                        b.FA_BF16, s0) == b.FA_ERR_SHAPE
+
+
+def test_binding_capacity_matches_the_header():
+    # the binding's copy of the scratch capacity is the header's #define
+    import os
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    with open(os.path.join(root, "include", "fa.h")) as f:
+        m = re.search(r"#define\s+FA_BWD_NOALLOC_MAX_ROWS\s+\(1LL\s*<<\s*(\d+)\)", f.read())
+    assert m, "FA_BWD_NOALLOC_MAX_ROWS not found in include/fa.h"
+    assert b.FA_BWD_NOALLOC_MAX_ROWS == 1 << int(m.group(1))
