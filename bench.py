@@ -1,19 +1,28 @@
 """Benchmark of the attention forward on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+                    [--workload NAME] [--split heads|strong|replicate]
+                    [--no-e2e] [--no-cpu-baseline] [--no-extras]
 
 One step is one fa_fwd launch over the whole workload (default: batch 8,
 32 heads, N = 8192, head dim 64, bf16, non-causal -- the headline shape of
 the pages' forward-time tables).  Inputs are seeded synthetic N(0, 1) data
 already resident in HBM; they are 805 MB, larger than the 129 MB L2, so
-no flush is needed between steps.  The metric is the attention-forward
-throughput, 4*B*H*N^2*d counted FLOPs per step (half when causal), in
-TFLOPS.  Prints one JSON line on rank 0.
+no flush is needed between steps (smaller workloads rotate through enough
+input sets that no step reads inputs left in L2 by the previous ones).
+The metric is the attention-forward throughput, 4*B*H*N^2*d counted FLOPs
+per step (half when causal), in TFLOPS.  Prints one JSON line on rank 0.
+At one GPU the line also carries ``extras``: short event-timed runs of the
+rest of the forward table (the N sweep 512..8192 causal and not, the fp16
+N = 512 case, the long-context d = 128 case, the e4m3 forward) and of the
+backward, each with its own kernel time, fraction of peak and clock record.
 
-Under torchrun (N > 1) every rank runs its own copy of the workload on its
-own GPU (independent (batch, head) problems: no data exchange); value is
-the FLOPs of all ranks over the slowest rank's time.
+Under torchrun (N > 1) the (batch, head) problems are split over the ranks
+with ``fwd_shard`` (no data exchange).  ``--split heads`` (default): the
+global workload has N times the batch, every rank computes its B*H share
+(weak scaling); ``--split strong``: the one workload is split (strong
+scaling); ``--split replicate``: every rank runs its own seeded copy.  value
+is the FLOPs of all ranks over the slowest rank's time.
 
 ``--impl reference`` times the fp64 CPU oracle on the host cores instead,
 on a bounded sample of the same workload per step (rank 0 only).
@@ -54,8 +63,7 @@ WORKLOADS = {w.name: w for w in
 DEFAULT_WORKLOAD = W.N8192.name
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from an
 # ncu capture of the kernel, keyed by a hash of the kernel sources and the
-# workload; reported only while the sources are unchanged (see
-# profiles/fa_fwd_kernel_b8h32n8192d64_bf16_launches.md).
+# workload; reported only while the sources are unchanged.
 MEASURED_TRAFFIC = {
     ("2e47b007cdb4836e", "b8h32n8192d64_bf16"): 805.49e6 + 253.82e6,
 }
@@ -189,13 +197,31 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+L2_BYTES = 129 * 10 ** 6
+
+
+def set_bytes(w):
+    """Bytes one step reads and writes: q, k, v, O and LSE."""
+    e = 1 if w.dtype == "e4m3" else 2
+    return w.B * w.H * ((w.N + 2 * w.n_keys) * w.d * e + w.N * w.d * 2 + 4 * w.N)
+
+
+def input_sets(w):
+    """How many separate input/output sets the timed steps rotate through so
+    that no step finds its inputs in the 129 MB L2: one when a set is larger
+    than twice the L2, else enough sets to pass more than twice the L2's
+    bytes between two uses of the same set."""
+    return max(1, -(-2 * L2_BYTES // set_bytes(w)))
+
+
 def l2_note(w):
-    """How the timed steps stand to the 129 MB L2: inputs larger than it need
-    no flush; smaller ones are timed warm, back to back, and say so."""
+    """How the timed steps stand to the 129 MB L2."""
     mb = (w.N + 2 * w.n_keys) * w.B * w.H * w.d * (1 if w.dtype == "e4m3" else 2) // 10 ** 6
-    if mb > 129:
+    n = input_sets(w)
+    if n == 1:
         return "inputs %d MB > 129 MB L2, no flush" % mb
-    return "inputs %d MB fit in the 129 MB L2: warm back-to-back steps, no flush" % mb
+    return ("inputs %d MB: %d input sets rotated (%d MB between reuses > 129 MB L2), "
+            "no flush" % (mb, n, n * set_bytes(w) // 10 ** 6))
 
 
 def time_oracle(w, budget_s, max_heads, rows_1t=256):
@@ -225,6 +251,122 @@ def time_oracle(w, budget_s, max_heads, rows_1t=256):
     one = time.perf_counter() - t0
     row_flops = 4.0 * w.n_keys * w.d / (2.0 if w.causal else 1.0)
     return secs, flops, heads, nt, row_flops * rows / one
+
+
+# ---------------------------------------------------------------- timing
+def time_launches(step, n_sets, warmup, steps, stream, local):
+    """Run ``step(i)`` (launching on ``stream``) ``warmup`` times untimed,
+    then ``steps`` times, each bracketed by CUDA events on ``stream``, while
+    nvidia-smi samples the clocks.  ``i`` cycles over ``n_sets`` input sets.
+    Returns (region ms, per-launch ms list, clock summary)."""
+    for i in range(warmup):
+        step(i % n_sets)
+    stream.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize(local)
+    with ClockSampler(local) as clocks:
+        for i in range(steps):
+            starts[i].record(stream)
+            step((warmup + i) % n_sets)
+            ends[i].record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize(local)
+    return (starts[0].elapsed_time(ends[-1]),
+            [s.elapsed_time(e) for s, e in zip(starts, ends)], clocks.summary())
+
+
+def fwd_step_fn(fa, w, sets, stream):
+    """One forward launch on input set i (fa_fwd, or fa_fwd_fp8 for e4m3)."""
+    fp8 = w.dtype == "e4m3"
+
+    def step(i):
+        q, k, v, o, lse = sets[i]
+        if fp8:
+            ds = W.E4M3_DESCALE
+            fa.fwd_fp8(q, k, v, ds, ds, ds, causal=w.causal, scale=w.scale,
+                       out=o, lse=lse, stream=stream)
+        else:
+            fa.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse,
+                   stream=stream)
+    return step
+
+
+def fwd_outputs(w, q):
+    o = torch.empty(q.shape, dtype=torch.bfloat16 if w.dtype == "e4m3" else q.dtype,
+                    device=q.device)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=q.device)
+    return o, lse
+
+
+def peak_tflops(fp8=False):
+    """The measured bf16 burst peak (x 2, the nominal fp8/bf16 dense ratio,
+    for e4m3 contractions) and a description of where it came from."""
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    desc = ("%s bf16 burst (MEASURED_PEAKS.json)" % src if src == "measured"
+            else "fallback 1.9 PFLOP/s bf16")
+    if fp8:
+        return 2.0 * peak, desc + " x 2 (nominal fp8/bf16 ratio)"
+    return peak, desc
+
+
+EXTRA_FWD = (W.sweep(False) + W.sweep(True)
+             + [W.N512, W.LONG, W.N8192_E4M3, W.N8192_E4M3_CAUSAL])
+EXTRA_BWD = [W.N2048, W.N2048_CAUSAL, W.N8192, W.N8192_CAUSAL, W.LONG]
+
+
+def run_extras(args, local):
+    """Short event-timed runs of the rest of the forward table and of the
+    backward, one record each (kernel time, TFLOPS, fraction of the peak,
+    clocks).  Inputs are drawn on the device (seeded); parity on these shapes
+    is the tests' business."""
+    import exact_attention_39_gb300 as fa
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    out = []
+    for w in EXTRA_FWD:
+        n = input_sets(w)
+        sets = []
+        for s in range(n):
+            q, k, v = W.make_inputs_on(w.with_(seed=w.seed + s), dev)
+            sets.append((q, k, v) + fwd_outputs(w, q))
+        _, ks, clk = time_launches(fwd_step_fn(fa, w, sets, stream), n, args.extra_warmup,
+                                   args.extra_steps, stream, local)
+        if fa.last_device_error(stream) != 0:
+            raise RuntimeError("device status set while timing %s" % w.name)
+        peak, _ = peak_tflops(w.dtype == "e4m3")
+        avg = sum(ks) / len(ks)
+        tf = w.flops() / (avg * 1e-3) / 1e12
+        out.append({"pass": "fwd", "workload": w.name, "B": w.B, "H": w.H, "N": w.N,
+                    "d": w.d, "dtype": w.dtype, "causal": w.causal,
+                    "kernel_ms": avg, "kernel_ms_median": sorted(ks)[len(ks) // 2],
+                    "tflops": tf, "frac": tf / peak, "l2": l2_note(w), "clocks": clk})
+        del sets
+    for w in EXTRA_BWD:
+        q, k, v = W.make_inputs_on(w, dev)
+        g = torch.randn(q.shape, generator=torch.Generator(device=dev).manual_seed(w.seed + 1000),
+                        device=dev).to(q.dtype)
+        o, lse = fa.fwd(q, k, v, causal=w.causal, scale=w.scale)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(fa.bwd_workspace_bytes(w.B, w.H, w.N), dtype=torch.uint8, device=dev)
+
+        def step(i):
+            fa.bwd(q, k, v, o, lse, g, causal=w.causal, scale=w.scale, dq=dq, dk=dk,
+                   dv=dv, workspace=ws, stream=stream)
+        _, ks, clk = time_launches(step, 1, args.extra_warmup, args.extra_steps, stream, local)
+        if fa.last_device_error(stream) != 0:
+            raise RuntimeError("device status set while timing the backward of %s" % w.name)
+        peak, _ = peak_tflops()
+        avg = sum(ks) / len(ks)
+        tf = 2.5 * w.flops() / (avg * 1e-3) / 1e12
+        out.append({"pass": "bwd", "workload": w.name, "B": w.B, "H": w.H, "N": w.N,
+                    "d": w.d, "dtype": w.dtype, "causal": w.causal,
+                    "kernel_ms": avg, "kernel_ms_median": sorted(ks)[len(ks) // 2],
+                    "tflops": tf, "frac": tf / peak,
+                    "flops_convention": "10*B*H*N^2*d, half causal", "clocks": clk})
+        del q, k, v, g, o, lse, dq, dk, dv, ws
+    return out
 
 
 # ---------------------------------------------------------------- arms
@@ -265,24 +407,37 @@ def run_reference(args, w, world, rank):
     }
 
 
+def standard_attention(q, k, v, causal, scale, out=None):
+    """Unfused attention with library calls, one batch element at a time:
+    S = scale * Q K^T materialised in the input dtype, the causal mask
+    (bottom-right aligned: key j visible to query i iff j <= i + Nk - Nq),
+    softmax in fp32, P rounded to the input dtype, O = P V.  q [B, H, Nq, d],
+    k and v [B, H, Nk, d]; returns O like q.  A query row that sees no key
+    (Nq > Nk, causal) has no softmax and comes out NaN."""
+    nq, nk = q.shape[2], k.shape[2]
+    o = torch.empty_like(q) if out is None else out
+    mask = None
+    if causal:
+        mask = torch.ones(nq, nk, dtype=torch.bool, device=q.device).tril(nk - nq)
+    for b in range(q.shape[0]):
+        s_ = torch.matmul(q[b], k[b].transpose(-1, -2)) * scale
+        if mask is not None:
+            s_ = s_.masked_fill(~mask, float("-inf"))
+        p_ = torch.softmax(s_.float(), dim=-1).to(q.dtype)
+        torch.matmul(p_, v[b], out=o[b])
+    return o
+
+
 def run_standard(args, w, world, rank, local):
-    """Unfused attention on the GPU with library calls: S = scale * Q K^T in
-    the input dtype, softmax in fp32, O = P V.  Same FLOP count as fa_fwd."""
+    """The unfused comparator on the GPU (torch/cuBLAS): same FLOP count as
+    fa_fwd."""
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     q, k, v = (t.to(dev) for t in W.make_inputs(w.with_(seed=w.seed + rank)))
     o = torch.empty_like(q)
-    mask = None
-    if w.causal:
-        mask = torch.ones(w.N, w.n_keys, dtype=torch.bool, device=dev).tril(w.n_keys - w.N)
 
     def step():
-        for b in range(w.B):
-            s_ = torch.matmul(q[b], k[b].transpose(-1, -2)) * w.scale
-            if mask is not None:
-                s_ = s_.masked_fill(~mask, float("-inf"))
-            p_ = torch.softmax(s_.float(), dim=-1).to(q.dtype)
-            torch.matmul(p_, v[b], out=o[b])
+        standard_attention(q, k, v, w.causal, w.scale, out=o)
 
     for _ in range(args.warmup):
         step()
@@ -325,30 +480,19 @@ def run_bwd(args, w, world, rank, local):
     ws = torch.empty(fa.bwd_workspace_bytes(w.B, w.H, w.N), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    def step():
+    def step(i):
         fa.bwd(q, k, v, o, lse, g, causal=w.causal, scale=w.scale, dq=dq, dk=dk,
                dv=dv, workspace=ws, stream=stream)
 
-    for _ in range(args.warmup):
-        step()
-    stream.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
     barrier(world)
-    with ClockSampler(local) as clocks:
-        t0.record(stream)
-        for _ in range(args.steps):
-            step()
-        t1.record(stream)
-        stream.synchronize()
+    region_ms, _, clk = time_launches(step, 1, args.warmup, args.steps, stream, local)
     if fa.last_device_error(stream) != 0:
         raise RuntimeError("device status set during the timed region")
     flops = 2.5 * w.flops()
-    ms, flops_all = aggregate(t0.elapsed_time(t1), flops * args.steps, world)
+    ms, flops_all = aggregate(region_ms, flops * args.steps, world)
     if rank != 0:
         return None
-    peaks, src = load_peaks()
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak, _ = peak_tflops()
     value = flops_all / (ms * 1e-3) / 1e12
     return {"pass": "bwd", "metric": "attn bwd TFLOPS (10*B*H*N^2*d counted FLOPs, "
             "half causal)", "value": value, "unit": UNIT, "n_gpus": world,
@@ -359,7 +503,29 @@ def run_bwd(args, w, world, rank, local):
                        "causal": w.causal},
             "gpu_launches": 3 * args.steps,
             "pct_of_peak": 100.0 * value / peak,
-            "clocks": clocks.summary()}
+            "clocks": clk}
+
+
+def split_plan(w, world, rank, mode):
+    """The problems rank ``rank`` of ``world`` computes under split ``mode``.
+
+    Returns (global workload, h0, h1, scaling): the rank computes the
+    flattened (batch, head) problems [h0, h1) of the global workload with
+    ``fwd_shard``.  "heads": the global workload has ``world`` times the
+    batch, so every rank's share is the B*H problems of ``w`` (weak
+    scaling); "strong": ``w`` itself is split; "replicate": every rank runs
+    all of ``w`` (its own seeded copy)."""
+    from exact_attention_39_gb300.shard import head_range
+    if mode == "replicate" or world == 1:
+        return w, 0, w.B * w.H, "weak"
+    if mode == "heads":
+        g = w.with_(B=w.B * world)
+        h0, h1 = head_range(g.B * g.H, world, rank)
+        return g, h0, h1, "weak"
+    if mode == "strong":
+        h0, h1 = head_range(w.B * w.H, world, rank)
+        return w, h0, h1, "strong"
+    raise ValueError("unknown split mode %r" % mode)
 
 
 def run_gpu(args, w, world, rank, local):
@@ -367,106 +533,122 @@ def run_gpu(args, w, world, rank, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wr = w.with_(seed=w.seed + rank)
-    q_h, k_h, v_h = W.make_inputs(wr)
-    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
     fp8 = w.dtype == "e4m3"
-    o = torch.empty(q.shape, dtype=torch.bfloat16 if fp8 else q.dtype, device=dev)
-    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
-
-    def step():
+    gw, h0, h1, scaling = split_plan(w, world, rank, args.split)
+    local_flops = w.flops() * (h1 - h0) / (w.B * w.H)   # this rank's share
+    sharded = world > 1 and args.split != "replicate"
+    if world == 1:
+        # the input recipe itself (CPU generator), as the parity tests draw it
+        q_h, k_h, v_h = W.make_inputs(w)
+    if sharded:
         if fp8:
-            ds = W.E4M3_DESCALE
-            fa.fwd_fp8(q, k, v, ds, ds, ds, causal=w.causal, scale=w.scale,
-                       out=o, lse=lse, stream=stream)
-        else:
-            fa.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse,
-                   stream=stream)
+            raise SystemExit("--split heads/strong shards the fp16/bf16 forward only")
+        # every rank holds the same global inputs and computes its problems
+        # [h0, h1) in place with fwd_shard
+        q, k, v = W.make_inputs_on(gw, dev)
+        n_sets = 1
+        o = torch.empty((h1 - h0, w.N, w.d), dtype=q.dtype, device=dev)
+        lse = torch.empty((h1 - h0, w.N), dtype=torch.float32, device=dev)
 
-    for _ in range(args.warmup):
-        step()
-    stream.synchronize()
-    if fa.last_device_error(stream) != 0:
-        raise RuntimeError("device status set during warm-up")
+        def step(i):
+            fa.fwd_shard(q, k, v, world, rank, causal=w.causal, scale=w.scale,
+                         stream=stream, out=o, lse=lse)
+    else:
+        n_sets = input_sets(w)
+        sets = []
+        for s in range(n_sets):
+            if world == 1 and s == 0:
+                q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+            else:
+                q, k, v = W.make_inputs_on(w.with_(seed=w.seed + 97 * rank + s), dev)
+            sets.append((q, k, v) + fwd_outputs(w, q))
+        q, k, v, o, lse = sets[0]
+        step = fwd_step_fn(fa, w, sets, stream)
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
-    torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clocks:
-        for i in range(args.steps):
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        stream.synchronize()
+    region_ms, kernel_ms, clk = time_launches(step, n_sets, args.warmup, args.steps,
+                                              stream, local)
     barrier(world)
-    torch.cuda.synchronize(dev)
-    region_ms = starts[0].elapsed_time(ends[-1])
-    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     if fa.last_device_error(stream) != 0:
         raise RuntimeError("device status set during the timed region")
 
-    ms, flops_all = aggregate(region_ms, w.flops() * args.steps, world)
+    ms, flops_all = aggregate(region_ms, local_flops * args.steps, world)
     value = flops_all / (ms * 1e-3) / 1e12
     ms_per_step = ms / args.steps
     kern_avg_ms = sum(kernel_ms) / len(kernel_ms)
 
     # ---- end to end through the public API: host buffers, copies timed
+    # (sharded: this rank's problems, uploaded into their places in the
+    # global device inputs)
     e2e = None
     if not args.no_e2e and not fp8:
+        if sharded:
+            flat = lambda t: t.reshape(gw.B * gw.H, *t.shape[2:])[h0:h1].unsqueeze(0)
+            qd, kd, vd = flat(q), flat(k), flat(v)
+            od, ld = o.unsqueeze(0), lse.unsqueeze(0)
+        else:
+            qd, kd, vd, od, ld = q, k, v, o, lse
+        if world > 1:
+            q_h, k_h, v_h = (t.cpu() for t in (qd, kd, vd))
         pin = [t.pin_memory() for t in (q_h, k_h, v_h)]
-        o_h = torch.empty_like(q_h).pin_memory()
-        l_h = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+        o_h = torch.empty_like(pin[0]).pin_memory()
+        l_h = torch.empty(tuple(ld.shape), dtype=torch.float32).pin_memory()
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
         for _ in range(2):
-            fa.fwd_host(*pin, q, k, v, o, lse, o_h, l_h, causal=w.causal,
+            fa.fwd_host(*pin, qd, kd, vd, od, ld, o_h, l_h, causal=w.causal,
                         scale=w.scale, stream=stream)
         barrier(world)
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
-            fa.fwd_host(*pin, q, k, v, o, lse, o_h, l_h, causal=w.causal,
+            fa.fwd_host(*pin, qd, kd, vd, od, ld, o_h, l_h, causal=w.causal,
                         scale=w.scale, stream=stream)
         e_ms = (time.perf_counter() - t0) * 1e3
         barrier(world)
-        e_ms, e_flops = aggregate(e_ms, w.flops() * e2e_steps, world)
+        e_ms, e_flops = aggregate(e_ms, local_flops * e2e_steps, world)
         h2d = sum(t.numel() * t.element_size() for t in pin)
         d2h = o_h.numel() * o_h.element_size() + l_h.numel() * l_h.element_size()
         e2e = {"value": e_flops / (e_ms * 1e-3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": e2e_steps, "ms_per_step": e_ms / e2e_steps}
 
+    extras = None
+    if world == 1 and not args.no_extras:
+        extras = run_extras(args, local)
+
     if rank != 0:
         return None
-    peaks, src = load_peaks()
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    # fp8 contractions: the measured bf16 peak times the nominal fp8/bf16
-    # dense ratio (4.5 / 2.25)
-    peak_mult = 2.0 if fp8 else 1.0
-    peak *= peak_mult
-    achieved = w.flops() / (kern_avg_ms * 1e-3) / 1e12
+    peak, peak_desc = peak_tflops(fp8)
+    achieved = local_flops / (kern_avg_ms * 1e-3) / 1e12
     kern_sorted = sorted(kernel_ms)
     kern_med = kern_sorted[len(kern_sorted) // 2]
     props = torch.cuda.get_device_properties(dev)
-    clk = clocks.summary()
     sm_mhz = clk.get("sm_mhz") or 0
     # one exponential per visible score: N*Nk per head, about half when causal
-    exps = w.B * w.H * w.N * w.n_keys / (2.0 if w.causal else 1.0)
+    exps = (h1 - h0) * w.N * w.n_keys / (2.0 if w.causal else 1.0)
+    key = (kernel_source_hash(), w.name)
+    traffic = args.traffic if args.traffic is not None else MEASURED_TRAFFIC.get(key)
+    if args.traffic is not None:
+        traffic_src = "given on the command line"
+    elif traffic is not None:
+        traffic_src = "ncu capture of this kernel source (hash %s)" % key[0]
+    else:
+        traffic_src = ("not measured for this kernel source (hash %s): no ncu capture "
+                       "since the kernel last changed" % key[0])
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": ("%s bf16 burst (MEASURED_PEAKS.json)" % src
-                                if src == "measured" else "fallback 1.9 PFLOP/s bf16")
-                + (" x 2 (nominal fp8/bf16 ratio)" if fp8 else ""),
-                "traffic": args.traffic if args.traffic is not None else
-                MEASURED_TRAFFIC.get((kernel_source_hash(), w.name)),
-                "algorithmic_bytes": w.hbm_bytes(),
+                "peak_source": peak_desc,
+                "traffic": traffic if world == 1 else None,
+                "traffic_source": traffic_src,
+                "algorithmic_bytes": w.hbm_bytes() * (h1 - h0) / (w.B * w.H),
                 "kernel_ms": kern_avg_ms,
                 "kernel_ms_median": kern_med, "kernel_ms_min": kern_sorted[0],
-                "pct_of_datasheet": 100.0 * achieved / (DATASHEET_TFLOPS * peak_mult),
+                "pct_of_datasheet": 100.0 * achieved / (DATASHEET_TFLOPS * (2 if fp8 else 1)),
                 "exp_per_clk_per_sm": (exps / (kern_avg_ms * 1e-3)
                                        / (sm_mhz * 1e6 * props.multi_processor_count)
                                        if sm_mhz else None),
-                "hbm_gbs_algorithmic": w.hbm_bytes() / (kern_avg_ms * 1e-3) / 1e9}
+                "hbm_gbs_algorithmic": w.hbm_bytes() * (h1 - h0) / (w.B * w.H)
+                / (kern_avg_ms * 1e-3) / 1e9}
     cpu = None
     if not args.no_cpu_baseline and world == 1:   # the CPU leg runs at N = 1 only
         secs, fl, heads, nt, one = time_oracle(w, args.cpu_budget, args.cpu_max_heads)
@@ -476,15 +658,21 @@ def run_gpu(args, w, world, rank, local):
                          % (heads, w.N, w.name, secs),
                "value_1_core": one / 1e12,
                "sample_1_core": "256 evenly spaced query rows of one head, 1 thread"}
-    return {
+    if world == 1:
+        par = "1 GPU"
+    elif args.split == "replicate":
+        par = "a seeded copy of the workload per GPU"
+    else:
+        par = "(batch, head) problems split over %d GPUs (fwd_shard, no collective)" % world
+    line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "higher_is_better": True, "scaling": scaling, "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                   "causal": w.causal, "global_batch": w.B * world,
-                   "seq_len": w.N, "parallelism": "independent heads per GPU" if world > 1 else "1 GPU",
-                   "l2": l2_note(w)},
+                   "causal": w.causal, "global_batch": gw.B if sharded else w.B * world,
+                   "seq_len": w.N, "parallelism": par, "split": args.split,
+                   "l2": l2_note(w) if not sharded else "inputs > 129 MB L2, no flush"},
         "gpu_launches": args.steps,
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": roofline,
@@ -492,6 +680,9 @@ def run_gpu(args, w, world, rank, local):
         "e2e": e2e,
         "clocks": clk,
     }
+    if extras is not None:
+        line["extras"] = extras
+    return line
 
 
 def main(argv=None):
@@ -503,12 +694,18 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="time the forward (default, the headline) or fa_bwd")
+    ap.add_argument("--split", choices=["heads", "strong", "replicate"], default="heads",
+                    help="how N > 1 ranks share the (batch, head) problems")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--cpu-max-heads", type=int, default=16)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other forward/backward shapes of the one-GPU line")
+    ap.add_argument("--extra-steps", type=int, default=20)
+    ap.add_argument("--extra-warmup", type=int, default=5)
     ap.add_argument("--ref-rows", type=int, default=1024,
                     help="query rows per reference step")
     ap.add_argument("--traffic", type=float, default=None,

@@ -137,6 +137,29 @@ def make_inputs(w, device="cpu"):
     return out
 
 
+def make_inputs_on(w, device):
+    """q, k, v of workload ``w`` drawn directly on ``device`` from a seeded
+    generator of that device: the same distribution, scaling and rounding as
+    ``make_inputs`` (the values differ from the CPU recipe's).  For timing
+    runs of shapes whose parity is checked with ``make_inputs`` inputs; it
+    saves drawing gigabytes on the host."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(w.seed))
+    dt = DTYPES[w.dtype]
+    shp_q = (w.B, w.H, w.N, w.d)
+    shp_k = (w.B, w.H, w.n_keys, w.d)
+    out = []
+    for shp, mult in ((shp_q, w.q_mult * w.in_mult), (shp_k, w.in_mult), (shp_k, w.in_mult)):
+        t = torch.randn(shp, generator=g, dtype=torch.float32, device=device)
+        if mult != 1.0:
+            t.mul_(mult)
+        if w.dtype == "e4m3":
+            t = (t / E4M3_DESCALE).clamp_(-448.0, 448.0)
+        out.append(t.to(dt))
+        del t
+    return tuple(out)
+
+
 def make_upstream_grad(w, seed_offset=1000):
     """dO for the backward: i.i.d. N(0, 1) like q, from its own seed."""
     g = torch.Generator(device="cpu")

@@ -125,7 +125,92 @@ def test_clock_summary_flags_throttling_and_missing_samples(tmp_path):
 def test_l2_note_names_the_flush_rule():
     assert "no flush" in bench.l2_note(bench.WORKLOADS["b8h32n8192d64_bf16"])
     assert "> 129 MB L2" in bench.l2_note(bench.WORKLOADS["b8h32n8192d64_bf16"])
-    assert "fit in the 129 MB L2" in bench.l2_note(bench.WORKLOADS["b8h32n512d64_fp16"])
+    assert "sets rotated" in bench.l2_note(bench.WORKLOADS["b8h32n512d64_fp16"])
+
+
+@pytest.mark.parametrize("name", sorted(bench.WORKLOADS))
+def test_input_sets_keep_every_step_out_of_l2(name):
+    # between two uses of one input set more than twice the L2's bytes pass
+    # (or one set alone is that large), so no timed step reads inputs the
+    # previous steps left in the 129 MB L2
+    w = bench.WORKLOADS[name]
+    n = bench.input_sets(w)
+    assert n >= 1 and n * bench.set_bytes(w) >= 2 * bench.L2_BYTES
+    if bench.set_bytes(w) >= 2 * bench.L2_BYTES:
+        assert n == 1
+    # the headline shape needs no rotation
+    assert bench.input_sets(bench.WORKLOADS["b8h32n8192d64_bf16"]) == 1
+    assert bench.set_bytes(bench.WORKLOADS["b8h32n8192d64_bf16"]) == \
+        bench.WORKLOADS["b8h32n8192d64_bf16"].hbm_bytes()
+
+
+def test_split_plan_modes():
+    w = bench.WORKLOADS["b8h32n8192d64_bf16"]
+    assert bench.split_plan(w, 1, 0, "heads") == (w, 0, 256, "weak")
+    g, h0, h1, sc = bench.split_plan(w, 4, 2, "heads")
+    assert g.B == 32 and (h0, h1) == (512, 768) and sc == "weak"
+    g, h0, h1, sc = bench.split_plan(w, 3, 2, "strong")
+    assert g is w and (h0, h1) == (171, 256) and sc == "strong"
+    assert bench.split_plan(w, 8, 5, "replicate") == (w, 0, 256, "weak")
+    with pytest.raises(ValueError):
+        bench.split_plan(w, 2, 0, "rows")
+
+
+def _split_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w = bench.WORKLOADS["b8h32n8192d64_bf16"]
+        for mode in ("heads", "strong"):
+            g, h0, h1, _ = bench.split_plan(w, world, rank, mode)
+            mine = torch.tensor([h0, h1, g.B * g.H], dtype=torch.int64)
+            every = [torch.zeros(3, dtype=torch.int64) for _ in range(world)]
+            dist.all_gather(every, mine)
+            q.put((rank, mode, [tuple(t.tolist()) for t in every]))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_split_the_timed_problems():
+    # the (batch, head) ranges the two ranks of the split modes time: they
+    # tile the global problems exactly once; "heads" keeps B*H per rank
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_split_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = [q.get(timeout=10) for _ in range(2 * world)]
+    for rank, mode, every in got:
+        total = every[0][2]
+        assert every[0][0] == 0 and every[-1][1] == total
+        assert all(a[1] == b[0] for a, b in zip(every, every[1:]))
+        if mode == "heads":
+            assert total == 2 * 256 and all(h1 - h0 == 256 for h0, h1, _ in every)
+        else:
+            assert total == 256 and all(h1 - h0 == 128 for h0, h1, _ in every)
+
+
+@pytest.mark.parametrize("dtype,tol", [("bf16", (2e-2, 2e-3)), ("fp16", (5e-3, 5e-4))])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("nq,nk", [(96, 96), (40, 96)])
+def test_standard_comparator_computes_attention_on_cpu(dtype, tol, causal, nq, nk):
+    # the unfused comparator (materialised S in the dtype, fp32 softmax)
+    # against the oracle, on CPU tensors: checks its arithmetic and its
+    # bottom-right causal mask
+    import numpy as np
+    import oracle
+    from exact_attention_39_gb300 import workloads as W
+    w = W.Workload("std", 1, 2, nq, 64, dtype, causal, seed=3, Nk=nk)
+    q, k, v = W.make_inputs(w)
+    o = bench.standard_attention(q, k, v, causal, w.scale)
+    o_ref, _ = oracle.attention_fwd(q.double().numpy(), k.double().numpy(),
+                                    v.double().numpy(), w.scale, causal)
+    err = np.abs(o.double().numpy() - o_ref)
+    assert err.max() <= tol[0] and err.mean() <= tol[1], (err.max(), err.mean())
 
 
 def test_peaks_fall_back_when_the_measured_file_is_absent(tmp_path, monkeypatch):
