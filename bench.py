@@ -198,6 +198,9 @@ class ClockSampler:
 
 
 L2_BYTES = 129 * 10 ** 6
+# GPU clock cycles of sleep per timed step enqueued ahead of a timed region
+# (about 100 us at 2 GHz: more than the host needs to enqueue one step)
+SLEEP_CYCLES_PER_STEP = 200000
 
 
 def set_bytes(w):
@@ -266,6 +269,12 @@ def time_launches(step, n_sets, warmup, steps, stream, local):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     torch.cuda.synchronize(local)
     with ClockSampler(local) as clocks:
+        # a short sleep kernel holds the stream while the host enqueues every
+        # timed launch, so launches run back to back and the events bracket
+        # the kernels, not the host's time to enqueue the next one (which can
+        # exceed a short kernel)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(SLEEP_CYCLES_PER_STEP * steps)
         for i in range(steps):
             starts[i].record(stream)
             step((warmup + i) % n_sets)
@@ -685,6 +694,19 @@ def run_gpu(args, w, world, rank, local):
     return line
 
 
+def parse_shape(text):
+    """"B,H,N,d,dtype[,causal]" -> a Workload named like the others."""
+    parts = [p.strip() for p in text.split(",")]
+    if len(parts) not in (5, 6) or parts[4] not in W.DTYPES:
+        raise SystemExit("--shape wants B,H,N,d,dtype[,causal], dtype one of %s"
+                         % ", ".join(sorted(W.DTYPES)))
+    B, H, N, d = (int(x) for x in parts[:4])
+    causal = len(parts) == 6 and parts[5].lower() in ("1", "causal", "true")
+    name = "b%dh%dn%dd%d_%s%s" % (B, H, N, d, parts[4], "_causal" if causal else "")
+    return W.Workload(name, B, H, N, d, parts[4], causal, seed=0,
+                      in_mult=0.5 if d == 128 else 1.0)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -692,6 +714,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference", "standard"], default="gb300")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--shape", default=None,
+                    help="B,H,N,d,dtype[,causal]: a workload of another shape (for "
+                         "profiling small cases); overrides --workload")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="time the forward (default, the headline) or fa_bwd")
     ap.add_argument("--split", choices=["heads", "strong", "replicate"], default="heads",
@@ -714,7 +739,7 @@ def main(argv=None):
     if args.warmup < 3 and args.impl == "gb300" and args.steps > 3:
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
     world, rank, local = dist_env()
-    w = WORKLOADS[args.workload]
+    w = WORKLOADS[args.workload] if args.shape is None else parse_shape(args.shape)
     if world > 1 and args.impl in ("gb300", "standard"):
         import torch.distributed as dist
         torch.cuda.set_device(local)

@@ -36,11 +36,15 @@ void *kernel_ptr() {
 }
 
 // Key lengths up to which D = 64 runs one query tile per CTA, two CTAs per
-// SM (CtaShape<1>): with at most four key blocks per CTA, overlapping one
-// CTA's set-up and epilogue with the other's work pays (measured at
-// B8 H32 N512: +12 % bf16, +18 % fp16); from eight blocks on the two-tile
-// CTA is faster (N1024: -4 %, N2048: -11 % with one tile).
+// SM (CtaShape<1>): with few key blocks per CTA, overlapping one CTA's
+// set-up and epilogue with the other's work pays (measured at B8 H32 N512:
+// +12 % bf16, +18 % fp16); from eight blocks on the two-tile CTA is faster
+// (N1024: -4 %, N2048: -11 % with one tile).  Causal units are shorter on
+// average (half the blocks), so the one-tile shape pays up to twice the keys
+// (B8 H32 N1024 causal: +12 % together with the longest-first order; N2048
+// causal: -7 %).
 constexpr int kOneTileMaxNk = 512;
+constexpr int kOneTileMaxNkCausal = 1024;
 
 // One-time, per-process and per-device set-up: the CUDA driver's
 // tensor-map encoder, the kernels' shared-memory opt-in, the status word's address.
@@ -202,7 +206,8 @@ fa_status run(const void *q, const void *k, const void *v, FwdParams p,
       !encode_map<D, T>(&mv, vb, nk_map, bh))
     return FA_ERR_CUDA;
   if constexpr (D == 64)
-    if (p.Nk <= kOneTileMaxNk) return run_shape<D, T, 1>(mq, mk, mv, p, bh, stream);
+    if (p.Nk <= kOneTileMaxNk || (p.causal && p.Nk <= kOneTileMaxNkCausal))
+      return run_shape<D, T, 1>(mq, mk, mv, p, bh, stream);
   return run_shape<D, T, 2>(mq, mk, mv, p, bh, stream);
 }
 

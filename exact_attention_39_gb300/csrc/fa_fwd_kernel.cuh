@@ -274,10 +274,20 @@ __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work unit: (head bh, 256-row unit), longest first when causal
-  const int bh = blockIdx.x / p.n_units;
-  int unit = blockIdx.x % p.n_units;
-  if (p.causal) unit = p.n_units - 1 - unit;
+  // ---- work unit: (head bh, unit of Q * 128 query rows).  Non-causal: the
+  // units of a head are consecutive, so the CTAs resident at one time share
+  // K/V blocks in L2.  Causal: units differ in length, so the grid runs the
+  // longest unit of every head first, then the next longest, and so on
+  // (longest-processing-time order keeps the tail short).
+  int bh, unit;
+  if (p.causal) {
+    const int nbh = (int)(gridDim.x / (unsigned)p.n_units);
+    bh = (int)(blockIdx.x % (unsigned)nbh);
+    unit = p.n_units - 1 - (int)(blockIdx.x / (unsigned)nbh);
+  } else {
+    bh = (int)(blockIdx.x / (unsigned)p.n_units);
+    unit = (int)(blockIdx.x % (unsigned)p.n_units);
+  }
   const int q0 = unit * kRowsPerCta;
   int kv_end = p.Nk;
   if (p.causal) kv_end = min(p.Nk, q0 + kRowsPerCta + (p.Nk - p.Nq));

@@ -230,3 +230,13 @@ def test_cpu_baseline_leg_counts_whole_heads():
     # a zero budget still times one whole head, then stops
     assert heads == 1 and secs > 0 and threads >= 1 and one > 0
     assert flops == w.with_(B=1, H=1).flops()
+
+
+def test_shape_option_names_the_workload():
+    w = bench.parse_shape("2,32,8192,64,bf16")
+    assert (w.B, w.H, w.N, w.d, w.dtype, w.causal) == (2, 32, 8192, 64, "bf16", False)
+    assert w.name == "b2h32n8192d64_bf16"
+    w = bench.parse_shape("1,4,1024,128,fp16,causal")
+    assert w.causal and w.name == "b1h4n1024d128_fp16_causal" and w.in_mult == 0.5
+    with pytest.raises(SystemExit):
+        bench.parse_shape("1,2,3")
