@@ -92,6 +92,7 @@ SWEEP_N = (512, 1024, 2048, 4096, 8192)
 
 N8192_E4M3 = N8192.with_(name="b8h32n8192d64_e4m3", dtype="e4m3")
 N8192_E4M3_CAUSAL = N8192_E4M3.with_(name="b8h32n8192d64_e4m3_causal", causal=True)
+LONG_E4M3 = LONG.with_(name="b1h32n32768d128_e4m3_causal", dtype="e4m3")
 
 
 def dequantized(t, dtype):

@@ -112,6 +112,17 @@ def test_fp8_headline_shape(w):
               rows=W.sample_rows(w.N, 512))
 
 
+@pytest.mark.gpu
+def test_fp8_long_context_d128():
+    # B1 H32 N32768 d128 causal (inputs N(0,1)/2), the shape where e4m3 runs
+    # faster than bf16: 2 sampled heads, 256 sampled query rows each
+    w = W.LONG_E4M3
+    q, k, v = W.make_inputs(w)
+    o, lse = run_fp8(w, q, k, v)
+    check_fp8(w, o, lse, q, k, v, heads=W.sample_heads(w, 2),
+              rows=W.sample_rows(w.N, 256))
+
+
 # ---------------------------------------------------------------- host side
 P = 0x10000
 
