@@ -30,9 +30,9 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 bool g_dev_ready[kMaxDevices] = {};
 unsigned *g_status_ptr[kMaxDevices] = {};
 
-template <int D, int T, int Q = 2>
+template <int D, int T, int Q = 2, bool kSkip = false>
 void *kernel_ptr() {
-  return reinterpret_cast<void *>(&fa_fwd_kernel<D, T, Q>);
+  return reinterpret_cast<void *>(&fa_fwd_kernel<D, T, Q, kSkip>);
 }
 
 // Key lengths up to which D = 64 runs one query tile per CTA, two CTAs per
@@ -79,6 +79,13 @@ fa_status ensure_ready(int dev) {
   for (int t = 0; t < 9; ++t) {
     if (cudaFuncSetAttribute(kernels[t], cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem[t]) != cudaSuccess)
+      return FA_ERR_CUDA;
+    // the causal two-tile d = 64 instantiations that skip tile 0's last block
+    if (t < 3 && cudaFuncSetAttribute(t == 0   ? kernel_ptr<64, kF16, 2, true>()
+                                      : t == 1 ? kernel_ptr<64, kBF16, 2, true>()
+                                               : kernel_ptr<64, kE4M3, 2, true>(),
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      smem[t]) != cudaSuccess)
       return FA_ERR_CUDA;
     // the one-tile shape needs room for two CTAs' shared memory per SM
     if (t >= 6 && cudaFuncSetAttribute(kernels[t],
@@ -191,9 +198,15 @@ fa_status run_shape(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensor
   cfg.blockDim = dim3(CtaShape<Q>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = Layout<D, T, Q>::kAlloc;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, T, Q>, mq, mk, mv, p) == cudaSuccess
-             ? FA_OK
-             : FA_ERR_CUDA;
+  cudaError_t e;
+  if constexpr (D == 64 && Q == 2) {
+    // causal: tile 0 skips a block past its diagonal (its own instantiation)
+    e = p.causal ? cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, T, Q, true>, mq, mk, mv, p)
+                 : cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, T, Q, false>, mq, mk, mv, p);
+  } else {
+    e = cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, T, Q>, mq, mk, mv, p);
+  }
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 template <int D, int T>

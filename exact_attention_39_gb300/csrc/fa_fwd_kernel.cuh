@@ -247,7 +247,11 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity,
   }
 }
 
-template <int D, int T, int Q>
+// kSkip (causal launches of the two-tile shape with merged barriers): a
+// tile that sees no key of the CTA's last block -- it lies wholly past the
+// tile's diagonal -- gets neither scores nor products for it.  A separate
+// instantiation, so that the others keep exactly their code.
+template <int D, int T, int Q, bool kSkip = false>
 __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK,
@@ -292,6 +296,13 @@ __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks
   int kv_end = p.Nk;
   if (p.causal) kv_end = min(p.Nk, q0 + kRowsPerCta + (p.Nk - p.Nq));
   const int nb = kv_end > 0 ? (kv_end + kBN - 1) / kBN : 0;
+  // Key blocks of query tile i (kSkip): those up to the block that holds its
+  // last row's diagonal (the last tile's are nb).
+  auto tile_blocks = [&](int i) -> int {
+    const int end = min(p.Nk, q0 + (i + 1) * kBM + (p.Nk - p.Nq));
+    return end > 0 ? (end + kBN - 1) / kBN : 0;
+  };
+  static_assert(!kSkip || (Layout<D, T, Q>::kMerged && Q == 2), "skip: merged two-tile shape");
 
   // ---- set-up: TMEM, barriers
   if (warp == kMmaWarp) {
@@ -427,6 +438,34 @@ __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks
       };
       bool ok = wait_warp(bar(L::bQFull), 0, abort_flag, p) &&
                 wait_warp(bar(L::bKFull + 0), 0, abort_flag, p);
+      if constexpr (kSkip) {
+        // tile 0 sees blocks 0 .. nb0-1, tile 1 all nb
+        const int nb0 = tile_blocks(0);
+        if (ok) {
+          ptx::tc_fence_after();
+          if (nb0 > 0) issue_s(0, 0);
+          issue_s(1, 0);
+        }
+        for (int j = 0; ok && j < nb; ++j) {
+          const int st = j % L::kStages;
+          const int st2 = (j + 1) % L::kStages;
+          if (j + 1 < nb) {
+            if (!wait_warp(bar(L::bKFull + st2), ((j + 1) / L::kStages) & 1, abort_flag, p) ||
+                !wait_warp(bar(L::bSFree), j & 1, abort_flag, p))
+              break;
+            ptx::tc_fence_after();
+            if (j + 1 < nb0) issue_s(0, st2);
+            issue_s(1, st2);
+          }
+          // both warpgroups have written P(j), or (tile 0 past its diagonal)
+          // arrived without one
+          if (!wait_warp(bar(L::bPFull), j & 1, abort_flag, p)) break;
+          ptx::tc_fence_after();
+          if (j < nb0) issue_pv(0, st, j > 0);
+          issue_pv(1, st, j > 0);
+          if (leader) ptx::mma_commit(bar(L::bKVEmpty + st));
+        }
+      } else {
       if (ok) {
         ptx::tc_fence_after();
         for (int i = 0; i < kNumQ; ++i) issue_s(i, 0);
@@ -485,6 +524,7 @@ __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks
           }
         }
       }
+      }
       // Every MMA issued has completed before TMEM is released.
       if (leader) ptx::mma_commit(bar(L::bDrain));
       wait_drain(bar(L::bDrain), 0, p);
@@ -508,7 +548,10 @@ __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks
     bool ok = true;
 
     const float2 c2 = make_float2(c, c);
-    for (int j = 0; j < nb; ++j) {
+    // blocks this tile sees (kSkip: tile 0 may see one fewer than the CTA)
+    int nb_i = nb;
+    if constexpr (kSkip) nb_i = tile_blocks(i);
+    for (int j = 0; j < nb_i; ++j) {
       if (!wait_phase(bar(L::bSFull + i), j & 1, abort_flag, p)) { ok = false; break; }
       ptx::tc_fence_after();
       uint32_t s[kBN];
@@ -618,8 +661,21 @@ __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks
       if (m_new != -CUDART_INF_F) m = m_use;
     }
 
+    if constexpr (kSkip) {
+      // Blocks nb_i .. nb-1 lie wholly past this tile's diagonal.  The merged
+      // "scores read" and "P written" barriers count both warpgroups, so this
+      // one still arrives on each, once the previous block's phase is
+      // complete (so that the arrivals count toward this block's phase).
+      for (int j = nb_i; ok && j < nb; ++j) {
+        if (!wait_phase(bar(L::bSFree), (j - 1) & 1, abort_flag, p)) { ok = false; break; }
+        ptx::mbar_arrive(bar(L::bSFree));
+        if (!wait_phase(bar(L::bPFull), (j - 1) & 1, abort_flag, p)) { ok = false; break; }
+        ptx::mbar_arrive(bar(L::bPFull));
+      }
+    }
+
     // ---- epilogue: O / l and LSE
-    if (ok && nb > 0) ok = wait_phase(bar(L::bODone + i), (nb - 1) & 1, abort_flag, p);
+    if (ok && nb_i > 0) ok = wait_phase(bar(L::bODone + i), (nb_i - 1) & 1, abort_flag, p);
     if (ok) {
       ptx::tc_fence_after();
       const bool valid = row < p.Nq;
@@ -629,7 +685,7 @@ __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
-        if (nb > 0) {
+        if (nb_i > 0) {
           ptx::tmem_ld32(tO + cc * 32, o);
           ptx::tmem_wait_ld();
           ptx::reg_fence32(o);

@@ -121,6 +121,24 @@ def test_ragged_lengths_d64(n, causal):
         full_check(w)
 
 
+# Causal problems with more than 1024 keys run the two-tile shape in which the
+# first tile skips a key block wholly past its diagonal; ragged lengths and
+# Nq != Nk move that block's position and the first tile's block count.
+@pytest.mark.parametrize("nq,nk", [(1025, 1025), (1100, 1100), (1281, 1281), (1500, 1500),
+                                   (2047, 2047), (2100, 2100), (1300, 1500), (1500, 1300),
+                                   (700, 1200), (1200, 1100), (260, 2049)])
+def test_causal_tile_skip_lengths(nq, nk):
+    for dtype in ("fp16", "bf16"):
+        w = W.Workload("skip", 1, 3, nq, 64, dtype, True, seed=nq + 7 * nk, Nk=nk)
+        q, k, v = W.make_inputs(w)
+        o, lse = run_gpu(w, q, k, v)
+        n_dead = max(0, nq - nk)
+        if n_dead:
+            assert (o[:, :, :n_dead] == 0).all()
+            assert torch.isinf(lse[:, :, :n_dead]).all()
+        check(w, o, lse, q, k, v, rows=list(range(n_dead, nq)))
+
+
 @pytest.mark.parametrize("n", [1, 100, 128, 256, 383, 512, 777])
 @pytest.mark.parametrize("causal", [False, True])
 def test_ragged_lengths_d128(n, causal):
