@@ -97,3 +97,25 @@ def test_shards_equal_the_whole_call(B, H, Nq, Nk, d, dtype, causal):
             assert torch.equal(o_r, o_flat[h0:h1]) and torch.equal(l_r, l_flat[h0:h1])
     torch.cuda.synchronize()
     assert fa.last_device_error() == 0
+
+
+@pytest.mark.gpu
+def test_shards_into_preallocated_outputs():
+    # the multi-GPU benchmark's call: each rank writes its problems into
+    # buffers it allocated once (weak split: the global batch is world x B)
+    w = W.Workload("shard_out", 4, 4, 2048, 64, "bf16", False, seed=23)
+    q, k, v = (t.cuda() for t in W.make_inputs(w))
+    o, lse = fa.fwd(q, k, v, scale=w.scale)
+    o_flat, l_flat = o.reshape(16, 2048, 64), lse.reshape(16, 2048)
+    world = 2
+    for rank in range(world):
+        h0, h1 = fa.head_range(16, world, rank)
+        out = torch.empty(h1 - h0, 2048, 64, dtype=q.dtype, device="cuda")
+        lse_r = torch.empty(h1 - h0, 2048, dtype=torch.float32, device="cuda")
+        o_r, l_r, rng = fa.fwd_shard(q, k, v, world, rank, scale=w.scale, out=out, lse=lse_r)
+        assert rng == (h0, h1) and o_r.data_ptr() == out.data_ptr()
+        assert torch.equal(out, o_flat[h0:h1]) and torch.equal(lse_r, l_flat[h0:h1])
+    with pytest.raises(ValueError):
+        fa.fwd_shard(q, k, v, world, 0, out=torch.empty(1, 2048, 64, dtype=q.dtype, device="cuda"))
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
