@@ -273,8 +273,10 @@ def time_launches(step, n_sets, warmup, steps, stream, local):
         # timed launch, so launches run back to back and the events bracket
         # the kernels, not the host's time to enqueue the next one (which can
         # exceed a short kernel)
-        with torch.cuda.stream(stream):
-            torch.cuda._sleep(SLEEP_CYCLES_PER_STEP * steps)
+        sleep = getattr(torch.cuda, "_sleep", None)   # torch's clock-bounded spin kernel
+        if sleep is not None:
+            with torch.cuda.stream(stream):
+                sleep(SLEEP_CYCLES_PER_STEP * steps)
         for i in range(steps):
             starts[i].record(stream)
             step((warmup + i) % n_sets)
