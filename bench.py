@@ -201,6 +201,7 @@ L2_BYTES = 129 * 10 ** 6
 # GPU clock cycles of sleep per timed step enqueued ahead of a timed region
 # (about 100 us at 2 GHz: more than the host needs to enqueue one step)
 SLEEP_CYCLES_PER_STEP = 200000
+SLEEP_CYCLES_MAX = 200000000                # about 0.1 s
 
 
 def set_bytes(w):
@@ -276,7 +277,7 @@ def time_launches(step, n_sets, warmup, steps, stream, local):
         sleep = getattr(torch.cuda, "_sleep", None)   # torch's clock-bounded spin kernel
         if sleep is not None:
             with torch.cuda.stream(stream):
-                sleep(SLEEP_CYCLES_PER_STEP * steps)
+                sleep(min(SLEEP_CYCLES_PER_STEP * steps, SLEEP_CYCLES_MAX))
         for i in range(steps):
             starts[i].record(stream)
             step((warmup + i) % n_sets)
