@@ -119,15 +119,17 @@ fa_status ensure_ready(int dev) {
 }
 
 // [BH, rows, d] tensor viewed by TMA as a 3-D box grid of (chunk width) x
-// 128 x 1 elements in the swizzle the kernel's layout names.  Rows past
+// box_rows x 1 elements in the swizzle the kernel's layout names (box_rows:
+// 128 for whole tiles, 64 for the backward's inner blocks).  Rows past
 // `rows` within a head read as zero.
 template <int D, int T>
-bool encode_map_uncached(CUtensorMap *map, const void *base, int rows, long long bh) {
+bool encode_map_uncached(CUtensorMap *map, const void *base, int rows, long long bh,
+                         int box_rows) {
   using L = Layout<D, T>;
   const cuuint64_t eb = (cuuint64_t)Elem<T>::kBytes;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)bh};
   cuuint64_t strides[2] = {(cuuint64_t)D * eb, (cuuint64_t)D * eb * (cuuint64_t)rows};
-  cuuint32_t box[3] = {(cuuint32_t)L::kChunkElems, (cuuint32_t)kBM, 1u};
+  cuuint32_t box[3] = {(cuuint32_t)L::kChunkElems, (cuuint32_t)box_rows, 1u};
   cuuint32_t estr[3] = {1u, 1u, 1u};
   const CUtensorMapDataType dt = T == kF16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                  : T == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
@@ -142,15 +144,16 @@ bool encode_map_uncached(CUtensorMap *map, const void *base, int rows, long long
 }
 
 // A tensor map depends only on (base address, rows, heads, head dim, element
-// type), so the maps of recent calls are kept and reused: a call on the same
-// buffers skips the driver's encoder.  Small and round-robin; a map is a
-// plain 128-byte value (no driver object to release).
+// type, box height), so the maps of recent calls are kept and reused: a call
+// on the same buffers skips the driver's encoder.  Small and round-robin; a
+// map is a plain 128-byte value (no driver object to release).
 struct MapKey {
   const void *base;
   long long bh;
-  int rows, d, t;
+  int rows, d, t, box_rows;
   bool operator==(const MapKey &o) const {
-    return base == o.base && bh == o.bh && rows == o.rows && d == o.d && t == o.t;
+    return base == o.base && bh == o.bh && rows == o.rows && d == o.d && t == o.t &&
+           box_rows == o.box_rows;
   }
 };
 struct MapEntry {
@@ -164,8 +167,9 @@ int g_map_next = 0;
 std::mutex g_map_mutex;
 
 template <int D, int T>
-bool encode_map(CUtensorMap *map, const void *base, int rows, long long bh) {
-  const MapKey key{base, bh, rows, D, T};
+bool encode_map(CUtensorMap *map, const void *base, int rows, long long bh,
+                int box_rows = kBM) {
+  const MapKey key{base, bh, rows, D, T, box_rows};
   {
     std::lock_guard<std::mutex> lock(g_map_mutex);
     for (const MapEntry &e : g_map_cache)
@@ -174,7 +178,7 @@ bool encode_map(CUtensorMap *map, const void *base, int rows, long long bh) {
         return true;
       }
   }
-  if (!encode_map_uncached<D, T>(map, base, rows, bh)) return false;
+  if (!encode_map_uncached<D, T>(map, base, rows, bh, box_rows)) return false;
   std::lock_guard<std::mutex> lock(g_map_mutex);
   MapEntry &e = g_map_cache[g_map_next];
   g_map_next = (g_map_next + 1) % kMapCacheSize;
@@ -286,13 +290,19 @@ __global__ void fa_selftest_wait_kernel(const WaitTestParams p) {
   wait_warp(b, 0, &abort_flag, p);
 }
 
-// Encodes the four maps and launches the three backward kernels.
+// Encodes the maps and launches the three backward kernels: the dQ kernel
+// reads Q and dO as 128-row tiles and K and V as 64-row blocks, the dK/dV
+// kernel the other way round.
 template <int D, int T>
 fa_status run_bwd(const void *q, const void *k, const void *v, const void *dout,
                   const BwdParams &p, long long bh, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mq_b, mk_b, mv_b, mdo_b;
   if (!encode_map<D, T>(&mq, q, p.Nq, bh) || !encode_map<D, T>(&mk, k, p.Nk, bh) ||
-      !encode_map<D, T>(&mv, v, p.Nk, bh) || !encode_map<D, T>(&mdo, dout, p.Nq, bh))
+      !encode_map<D, T>(&mv, v, p.Nk, bh) || !encode_map<D, T>(&mdo, dout, p.Nq, bh) ||
+      !encode_map<D, T>(&mq_b, q, p.Nq, bh, kBwdBlk) ||
+      !encode_map<D, T>(&mk_b, k, p.Nk, bh, kBwdBlk) ||
+      !encode_map<D, T>(&mv_b, v, p.Nk, bh, kBwdBlk) ||
+      !encode_map<D, T>(&mdo_b, dout, p.Nq, bh, kBwdBlk))
     return FA_ERR_CUDA;
   const long long rows_pad = bh * (long long)p.n_pad;
   const long long threads = rows_pad * 8;
@@ -303,11 +313,11 @@ fa_status run_bwd(const void *q, const void *k, const void *v, const void *dout,
   cfg.stream = stream;
   cfg.gridDim = dim3((unsigned)(bh * p.n_qblk), 1, 1);
   cfg.dynamicSmemBytes = BwdQLayout<D, T>::kAlloc;
-  if (cudaLaunchKernelEx(&cfg, fa_bwd_dq_kernel<D, T>, mq, mk, mv, mdo, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, fa_bwd_dq_kernel<D, T>, mq, mk_b, mv_b, mdo, p) != cudaSuccess)
     return FA_ERR_CUDA;
   cfg.gridDim = dim3((unsigned)(bh * p.n_kblk), 1, 1);
   cfg.dynamicSmemBytes = BwdKVLayout<D, T>::kAlloc;
-  if (cudaLaunchKernelEx(&cfg, fa_bwd_dkdv_kernel<D, T>, mq, mk, mv, mdo, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, fa_bwd_dkdv_kernel<D, T>, mq_b, mk, mv, mdo_b, p) != cudaSuccess)
     return FA_ERR_CUDA;
   return FA_OK;
 }

@@ -16,16 +16,33 @@
 //                       blocks (0 and -inf on padding, so its probabilities
 //                       are zero); negated so that the element-wise steps
 //                       are packed two-wide adds and fused multiply-adds
-//   fa_bwd_dq_kernel    one CTA per 128 query rows, looping over key blocks:
-//                       S = Q K^T and dP = dO V^T into TMEM, dS to TMEM,
-//                       dQ += dS K (K read as the MN-major B operand)
-//   fa_bwd_dkdv_kernel  one CTA per 128 keys, looping over query blocks:
-//                       S^T = K Q^T and dP^T = V dO^T (keys on TMEM lanes),
-//                       P^T and dS^T to TMEM, dV += P^T dO, dK += dS^T Q
+//   fa_bwd_dq_kernel    one CTA per 128 query rows, looping over 64-key
+//                       blocks: S = Q K^T and dP = dO V^T into TMEM, dS over
+//                       dP, dQ += dS K (K read as the MN-major B operand)
+//   fa_bwd_dkdv_kernel  one CTA per 128 keys, looping over 64-row query
+//                       blocks: S^T = K Q^T and dP^T = V dO^T (keys on TMEM
+//                       lanes), P^T over S^T and dS^T over dP^T, dV += P^T dO,
+//                       dK += dS^T Q
 // Both main kernels: warps 0-7 element-wise in two warpgroups (thread = TMEM
-// lane; warpgroup h takes columns 64h .. 64h+63 of each 128-column block and
+// lane; warpgroup h takes columns 32h .. 32h+31 of each 64-column block and
 // half of the output columns), warp 8 TMA producer, warp 9 TMEM allocator
-// and MMA issuer.  No row reduction crosses the halves.
+// and MMA issuer (the whole warp runs the loop, one elected lane issues).
+//
+// Pipelining.  S and dP of a block live in one of kBuf TMEM buffers; the
+// MMA thread issues the gradient product of block n and then, into the same
+// buffer, the scores of block n + kBuf.  The tensor pipe runs one thread's
+// MMAs in issue order, so the product has read P (or dS) before the next
+// scores overwrite it, and an element-wise thread that sees block n + kBuf's
+// scores complete knows that block n's product is done with its columns.
+// While the element-wise warps work on block n the pipe has the products of
+// the blocks in between to run; nothing waits on a round trip per block.
+//
+// The operand that stays fixed over a CTA's loop (Q and dO in the dQ kernel;
+// K and V in the dK/dV kernel for D = 64) is copied once from shared memory
+// into TMEM by the element-wise warps and read from there as the A operand:
+// with both operands in shared memory an M = 128, N = 64 MMA is held to the
+// shared-memory read rate (6 KB per MMA, 48 cycles instead of 32 on the
+// GB300); with A in TMEM it runs at the tensor pipe's rate.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -40,7 +57,8 @@ constexpr int kBwdThreads = 320;
 constexpr int kBwdLoadWarp = 8;
 constexpr int kBwdMmaWarp = 9;
 constexpr int kBwdEwThreads = 256;       // element-wise threads
-constexpr int kBwdHalf = 64;             // columns per element-wise thread
+constexpr int kBwdBlk = 64;              // inner block: query rows (dK/dV) or keys (dQ)
+constexpr int kBwdHalf = kBwdBlk / 2;    // columns of a block per element-wise thread
 
 struct BwdParams {
   const void *o, *dout;      // [BH, Nq, D]
@@ -111,65 +129,89 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+
 // ---------------------------------------------------------------- layouts
+// A 64-row block tile (Q and dO blocks of the dK/dV kernel, K and V blocks
+// of the dQ kernel): the same 128-byte-swizzled chunks as a 128-row tile,
+// each chunk kBwdBlk rows high.
+template <int D, int T>
+struct BlkTile {
+  using F = Layout<D, T>;
+  static constexpr int kChunkBytes = kBwdBlk * F::kSwz;
+  static constexpr int kBytes = F::kChunks * kChunkBytes;
+};
+
 template <int D, int T>
 struct BwdQLayout {
   using F = Layout<D, T>;
-  static constexpr int kTile = F::kTileBytes;
-  // D = 64: four stages, K and V of a stage on one barrier, and one "S and
-  // dP read" wait per block gating both the next S, dP and the previous
-  // block's dQ product (the loads then have two blocks of lead time).
-  static constexpr bool kMerged = kTile <= 16384;
-  static constexpr int kStages = kMerged ? 4 : 2;
-  static constexpr int kQ = 0;                           // Q tile
-  static constexpr int kdO = kTile;                      // dO tile
-  static constexpr int kK = 2 * kTile;                   // K ring
-  static constexpr int kV = kK + kStages * kTile;        // V ring
-  static constexpr int kBars = kV + kStages * kTile;
+  using H = BlkTile<D, T>;
+  static constexpr int kTile = F::kTileBytes;            // Q, dO: 128 rows
+  static constexpr int kStages = D == 64 ? 8 : 4;        // K, V block ring
+  static constexpr int kBuf = D == 64 ? 3 : 2;           // S, dP buffers in TMEM
+  static constexpr int kQ = 0;
+  static constexpr int kdO = kTile;
+  static constexpr int kRing = 2 * kTile;
+  static constexpr int kStageBytes = 2 * H::kBytes;      // K block, V block
+  static constexpr int kBars = kRing + kStages * kStageBytes;
   static constexpr int bQFull = 0;
-  static constexpr int bKFull = 1;
-  static constexpr int bVFull = bKFull + kStages;
-  static constexpr int bKVEmpty = bVFull + kStages;
-  static constexpr int bSFull = bKVEmpty + kStages;      // S and dP ready
-  static constexpr int bSFree = bSFull + 1;              // S and dP read
-  static constexpr int bDSFull = bSFree + 1;             // dS written
-  static constexpr int bDQDone = bDSFull + 1;            // [2]: dQ MMA done
-  static constexpr int bDrain = bDQDone + 2;
+  static constexpr int bKVFull = 1;                      // [stages]
+  static constexpr int bKVEmpty = bKVFull + kStages;     // [stages]
+  static constexpr int bSFull = bKVEmpty + kStages;      // [kBuf]: S and dP done
+  static constexpr int bDSFull = bSFull + kBuf;          // [kBuf]: dS written
+  static constexpr int bAFull = bDSFull + kBuf;          // Q, dO copied into TMEM
+  static constexpr int bGDone = bAFull + 1;              // every dQ product done
+  static constexpr int bDrain = bGDone + 1;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kAlloc = kMisc + 16 + 1024;
-  // TMEM columns
-  static constexpr uint32_t tS = 0, tdP = 128, tdQ = 256;
-  __host__ __device__ static constexpr uint32_t tdS(int b) { return 256 + D + 64 * b; }
+  __host__ __device__ static constexpr int stage(int s) { return kRing + s * kStageBytes; }
+  // TMEM columns: S(b), dP(b) (dS over the first columns of each half),
+  // the dQ accumulator, then Q and dO as 16-bit pairs
+  __host__ __device__ static constexpr uint32_t tS(int b) { return 64u * b; }
+  __host__ __device__ static constexpr uint32_t tdP(int b) { return 64u * (kBuf + b); }
+  static constexpr uint32_t tdQ = 128u * kBuf;
+  static constexpr uint32_t tQa = tdQ + D;
+  static constexpr uint32_t tdOa = tQa + D / 2;
+  static_assert(tdOa + D / 2 <= (uint32_t)kTmemCols, "TMEM columns");
+  static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
 
 template <int D, int T>
 struct BwdKVLayout {
   using F = Layout<D, T>;
-  static constexpr int kTile = F::kTileBytes;
-  static constexpr int kStageBytes = 2 * kTile + 2 * kBM * 4;   // Q, dO, LSE, D
-  static constexpr int kStages = kTile <= 16384 ? 4 : 2;
+  using H = BlkTile<D, T>;
+  // D = 64: K and V as TMEM A operands (every product an A-in-TMEM MMA).
+  // D = 128: the accumulators take half of TMEM and K, V stay in shared
+  // memory (S^T and dP^T then read both operands from there).
+  static constexpr bool kATmem = D == 64;
+  static constexpr int kTile = F::kTileBytes;            // K, V: 128 rows
+  // Q block, dO block, then 64 floats of -LSE and 64 of -D (1 KB-aligned)
+  static constexpr int kStageBytes = 2 * H::kBytes + 1024;
+  static constexpr int kStages = D == 64 ? 8 : 4;
+  static constexpr int kBuf = 2;
   static constexpr int kK = 0, kV = kTile;
   static constexpr int kStage0 = 2 * kTile;
   static constexpr int kBars = kStage0 + kStages * kStageBytes;
   static constexpr int bKVFull = 0;
   static constexpr int bQFull = 1;                       // [stages]
   static constexpr int bQEmpty = bQFull + kStages;       // [stages]
-  static constexpr int bSFull = bQEmpty + kStages;       // S^T and dP^T ready
-  static constexpr int bSFree = bSFull + 1;
-  static constexpr int bPFull = bSFree + 1;              // P^T, dS^T written
-  static constexpr int bPDone = bPFull + 1;              // dV, dK MMAs done
-  static constexpr int bDrain = bPDone + 1;
+  static constexpr int bSFull = bQEmpty + kStages;       // [kBuf]: S^T, dP^T done
+  static constexpr int bPFull = bSFull + kBuf;           // [kBuf]: P^T, dS^T written
+  static constexpr int bAFull = bPFull + kBuf;           // K, V copied into TMEM
+  static constexpr int bGDone = bAFull + 1;              // every dV, dK product done
+  static constexpr int bDrain = bGDone + 1;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kAlloc = kMisc + 16 + 1024;
-  // P^T and dS^T fit beside the accumulators for D = 64; for D = 128 they
-  // overwrite the first 64 columns of S^T and dP^T once those are read.
-  static constexpr bool kEarly = D == 64;
-  static constexpr uint32_t tS = 0, tdP = 128, tdV = 256, tdK = 256 + D;
-  static constexpr uint32_t tP = kEarly ? 384 : 0;
-  static constexpr uint32_t tdS = kEarly ? 448 : 128;
   __host__ __device__ static constexpr int stage(int s) { return kStage0 + s * kStageBytes; }
+  __host__ __device__ static constexpr uint32_t tS(int b) { return 64u * b; }
+  __host__ __device__ static constexpr uint32_t tdP(int b) { return 64u * (kBuf + b); }
+  static constexpr uint32_t tdV = 128u * kBuf;
+  static constexpr uint32_t tdK = tdV + D;
+  static constexpr uint32_t tKa = tdK + D;               // kATmem only
+  static constexpr uint32_t tVa = tKa + D / 2;
+  static_assert((kATmem ? tVa + D / 2 : tdK + D) <= (uint32_t)kTmemCols, "TMEM columns");
+  static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
 
 // 16-bit pair packing of the element type
@@ -191,17 +233,49 @@ __device__ __forceinline__ BwdSmem bwd_smem(uint8_t *smem_raw) {
   return {sbase, smem_raw + (sbase - raw)};
 }
 
+// Copies row r of a 128-row tile (chunks of 128 rows x 128 bytes in the TMA
+// 128-byte swizzle) into the calling thread's TMEM lane: D/2 columns of
+// 16-bit pairs, element 2c in the low half of column c -- the layout of an
+// A operand in TMEM.
+template <int D, int T>
+__device__ __forceinline__ void tile_row_to_tmem(const uint8_t *tile, int r, uint32_t taddr) {
+  using F = Layout<D, T>;
+  static_assert(F::kSwz == 128, "128-byte rows");
+#pragma unroll
+  for (int c = 0; c < F::kChunks; ++c) {
+    uint32_t w[32];
+    const uint8_t *row = tile + c * F::kChunkBytes + r * 128;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint4 x = *reinterpret_cast<const uint4 *>(row + ((u ^ (r & 7)) << 4));
+      w[4 * u] = x.x;
+      w[4 * u + 1] = x.y;
+      w[4 * u + 2] = x.z;
+      w[4 * u + 3] = x.w;
+    }
+    ptx::tmem_st32(taddr + 32u * c, w);
+  }
+}
+
+// The A columns of K step kk (16 elements) of a 64-column block whose two
+// halves (32 elements, 16 columns of pairs) sit at +0 and +32.
+__device__ __forceinline__ constexpr uint32_t half_cols(int kk) {
+  return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8);
+}
+
 // ---------------------------------------------------------------- dQ
 template <int D, int T>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,
-                     const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV,
-                     const __grid_constant__ CUtensorMap tmdO,
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ,     // 128-row boxes
+                     const __grid_constant__ CUtensorMap tmK,     // 64-row boxes
+                     const __grid_constant__ CUtensorMap tmV,     // 64-row boxes
+                     const __grid_constant__ CUtensorMap tmdO,    // 128-row boxes
                      const BwdParams p) {
   using L = BwdQLayout<D, T>;
   using F = typename L::F;
+  using H = typename L::H;
   using E = Elem<T>;
+  constexpr int kBuf = L::kBuf;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const BwdSmem sm = bwd_smem(smem_raw);
   const uint32_t sbase = sm.sbase;
@@ -217,7 +291,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int q0 = qb * kBM;
   int kv_end = p.Nk;
   if (p.causal) kv_end = min(p.Nk, q0 + kBM + (p.Nk - p.Nq));
-  const int nb = kv_end > 0 ? (kv_end + kBN - 1) / kBN : 0;
+  const int nb = kv_end > 0 ? (kv_end + kBwdBlk - 1) / kBwdBlk : 0;   // 64-key blocks
 
   if (warp == kBwdMmaWarp) {
     ptx::tmem_alloc(sbase + L::kMisc, kTmemCols);
@@ -226,15 +300,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(L::bQFull), 1);
     for (int s = 0; s < L::kStages; ++s) {
-      ptx::mbar_init(bar(L::bKFull + s), 1);
-      ptx::mbar_init(bar(L::bVFull + s), 1);
+      ptx::mbar_init(bar(L::bKVFull + s), 1);
       ptx::mbar_init(bar(L::bKVEmpty + s), 1);
     }
-    ptx::mbar_init(bar(L::bSFull), 1);
-    ptx::mbar_init(bar(L::bSFree), kBwdEwThreads);
-    ptx::mbar_init(bar(L::bDSFull), kBwdEwThreads);
-    ptx::mbar_init(bar(L::bDQDone), 1);
-    ptx::mbar_init(bar(L::bDQDone + 1), 1);
+    for (int b = 0; b < kBuf; ++b) {
+      ptx::mbar_init(bar(L::bSFull + b), 1);
+      ptx::mbar_init(bar(L::bDSFull + b), kBwdEwThreads);
+    }
+    ptx::mbar_init(bar(L::bAFull), kBwdEwThreads);
+    ptx::mbar_init(bar(L::bGDone), 1);
     ptx::mbar_init(bar(L::bDrain), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -264,14 +338,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int st = j % L::kStages, use = j / L::kStages;
         if (use > 0 && !wait_warp(bar(L::bKVEmpty + st), (use - 1) & 1, abort_flag, p)) break;
         if (leader) {
-          const uint32_t vbar = bar(L::kMerged ? L::bKFull + st : L::bVFull + st);
-          ptx::mbar_arrive_expect_tx(bar(L::bKFull + st), L::kMerged ? 2 * L::kTile : L::kTile);
-          if (!L::kMerged) ptx::mbar_arrive_expect_tx(vbar, L::kTile);
+          const uint32_t sa = sbase + L::stage(st);
+          ptx::mbar_arrive_expect_tx(bar(L::bKVFull + st), 2 * H::kBytes);
           for (int c = 0; c < F::kChunks; ++c) {
-            ptx::tma_load_3d(sbase + L::kK + st * L::kTile + c * F::kChunkBytes, &tmK,
-                             bar(L::bKFull + st), c * F::kChunkElems, j * kBN, bh, pol_kv);
-            ptx::tma_load_3d(sbase + L::kV + st * L::kTile + c * F::kChunkBytes, &tmV,
-                             vbar, c * F::kChunkElems, j * kBN, bh, pol_kv);
+            ptx::tma_load_3d(sa + c * H::kChunkBytes, &tmK, bar(L::bKVFull + st),
+                             c * F::kChunkElems, j * kBwdBlk, bh, pol_kv);
+            ptx::tma_load_3d(sa + H::kBytes + c * H::kChunkBytes, &tmV, bar(L::bKVFull + st),
+                             c * F::kChunkElems, j * kBwdBlk, bh, pol_kv);
           }
         }
         issued = j + 1;
@@ -279,97 +352,71 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       wait_drain(bar(L::bQFull), 0, p);
       for (int j = issued - L::kStages; j < issued; ++j) {
         if (j < 0) continue;
-        const int st = j % L::kStages;
-        const uint32_t ph = (uint32_t)(j / L::kStages) & 1u;
-        wait_drain(bar(L::bKFull + st), ph, p);
-        if (!L::kMerged) wait_drain(bar(L::bVFull + st), ph, p);
+        wait_drain(bar(L::bKVFull + j % L::kStages), (uint32_t)(j / L::kStages) & 1u, p);
       }
     }
   } else if (warp == kBwdMmaWarp) {
     // ================================================= MMA issuer
     if (nb > 0) {
       const bool leader = ptx::elect_one();
-      constexpr uint32_t idesc_s = make_idesc(kBM, kBN, E::kFmt, false);
+      constexpr uint32_t idesc_s = make_idesc(kBM, kBwdBlk, E::kFmt, false);
       constexpr uint32_t idesc_q = make_idesc(kBM, D, E::kFmt, true);
-      const uint64_t dq_ = make_sdesc(sbase + L::kQ, 16, F::kSBO, F::kSwzMode);
-      const uint64_t ddo = make_sdesc(sbase + L::kdO, 16, F::kSBO, F::kSwzMode);
-      const uint64_t dk0 = make_sdesc(sbase + L::kK, 16, F::kSBO, F::kSwzMode);
-      const uint64_t dv0 = make_sdesc(sbase + L::kV, 16, F::kSBO, F::kSwzMode);
-      const uint64_t dkmn0 = make_sdesc(sbase + L::kK, F::kChunkBytes, F::kSBO, F::kSwzMode);
-      // S = Q K_st^T and dP = dO V_st^T, then a commit on s_full
-      auto issue_s = [&](int st) {
-        const uint64_t dk = dk0 + (uint64_t)((st * L::kTile) >> 4);
-        const uint64_t dv = dv0 + (uint64_t)((st * L::kTile) >> 4);
+      const uint64_t dk0 = make_sdesc(sbase + L::stage(0), 16, F::kSBO, F::kSwzMode);
+      const uint64_t dv0 = make_sdesc(sbase + L::stage(0) + H::kBytes, 16, F::kSBO, F::kSwzMode);
+      const uint64_t dkmn0 = make_sdesc(sbase + L::stage(0), H::kChunkBytes, F::kSBO, F::kSwzMode);
+      // S(b) = Q K_st^T and dP(b) = dO V_st^T, then a commit on s_full[b]
+      auto issue_s = [&](int st, int b) {
+        const uint64_t so = (uint64_t)((st * L::kStageBytes) >> 4);
         if (leader) {
-          // all of S's steps, then all of dP's (one accumulator at a time)
 #pragma unroll
           for (int kk = 0; kk < D / E::kMmaK; ++kk) {
-            const uint32_t off = ((kk >> 2) * F::kChunkBytes + (kk & 3) * 32) >> 4;
-            ptx::mma_ss(tmem + L::tS, dq_ + off, dk + off, idesc_s, kk > 0);
+            const uint32_t off = ((kk >> 2) * H::kChunkBytes + (kk & 3) * 32) >> 4;
+            ptx::mma_ts(tmem + L::tS(b), tmem + L::tQa + kk * 8, dk0 + so + off, idesc_s, kk > 0);
           }
 #pragma unroll
           for (int kk = 0; kk < D / E::kMmaK; ++kk) {
-            const uint32_t off = ((kk >> 2) * F::kChunkBytes + (kk & 3) * 32) >> 4;
-            ptx::mma_ss(tmem + L::tdP, ddo + off, dv + off, idesc_s, kk > 0);
+            const uint32_t off = ((kk >> 2) * H::kChunkBytes + (kk & 3) * 32) >> 4;
+            ptx::mma_ts(tmem + L::tdP(b), tmem + L::tdOa + kk * 8, dv0 + so + off, idesc_s,
+                        kk > 0);
           }
-          ptx::mma_commit(bar(L::bSFull));
+          ptx::mma_commit(bar(L::bSFull + b));
         }
       };
-      // dQ (+)= dS_b K_st, then commits on dq_done[b] and kv_empty[st]
+      // dQ (+)= dS(b) K_st, then a commit on kv_empty[st]
       auto issue_dq = [&](int st, int b, bool acc) {
-        const uint64_t dk = dkmn0 + (uint64_t)((st * L::kTile) >> 4);
+        const uint64_t so = (uint64_t)((st * L::kStageBytes) >> 4);
         if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < kBN / E::kMmaK; ++kk)
-            ptx::mma_ts(tmem + L::tdQ, tmem + L::tdS(b) + kk * 8,
-                        dk + (uint64_t)((kk * E::kMmaK * F::kSwz) >> 4), idesc_q,
+          for (int kk = 0; kk < kBwdBlk / E::kMmaK; ++kk)
+            ptx::mma_ts(tmem + L::tdQ, tmem + L::tdP(b) + half_cols(kk),
+                        dkmn0 + so + (uint64_t)((kk * E::kMmaK * F::kSwz) >> 4), idesc_q,
                         (acc || kk > 0) ? 1u : 0u);
-          ptx::mma_commit(bar(L::bDQDone + b));
           ptx::mma_commit(bar(L::bKVEmpty + st));
         }
       };
-      bool ok = wait_warp(bar(L::bQFull), 0, abort_flag, p) &&
-                wait_warp(bar(L::bKFull), 0, abort_flag, p) &&
-                (L::kMerged || wait_warp(bar(L::bVFull), 0, abort_flag, p));
-      if (ok) {
+      bool ok = wait_warp(bar(L::bAFull), 0, abort_flag, p);
+      for (int j = 0; ok && j < kBuf && j < nb; ++j) {
+        if (!wait_warp(bar(L::bKVFull + j), 0, abort_flag, p)) { ok = false; break; }
         ptx::tc_fence_after();
-        issue_s(0);
+        issue_s(j, j);
       }
-      if constexpr (L::kMerged) {
-        for (int j = 0; ok && j < nb; ++j) {
-          const int st2 = (j + 1) % L::kStages;
-          if (j + 1 < nb &&
-              !wait_warp(bar(L::bKFull + st2), ((j + 1) / L::kStages) & 1, abort_flag, p)) {
+      for (int j = 0; ok && j < nb; ++j) {
+        const int b = j % kBuf;
+        if (!wait_warp(bar(L::bDSFull + b), (j / kBuf) & 1, abort_flag, p)) { ok = false; break; }
+        ptx::tc_fence_after();
+        issue_dq(j % L::kStages, b, j > 0);
+        const int m = j + kBuf;   // into the buffer just read
+        if (m < nb) {
+          const int st = m % L::kStages;
+          if (!wait_warp(bar(L::bKVFull + st), (m / L::kStages) & 1, abort_flag, p)) {
             ok = false;
             break;
           }
-          // S(j), dP(j) are in registers; dS(j-1) was written before that
-          if (!wait_warp(bar(L::bSFree), j & 1, abort_flag, p)) { ok = false; break; }
           ptx::tc_fence_after();
-          if (j + 1 < nb) issue_s(st2);
-          if (j > 0) issue_dq((j - 1) % L::kStages, (j - 1) & 1, j > 1);
-        }
-        // the last block's dQ product once its dS is written
-        if (ok && wait_warp(bar(L::bDSFull), 0, abort_flag, p)) {
-          ptx::tc_fence_after();
-          issue_dq((nb - 1) % L::kStages, (nb - 1) & 1, nb > 1);
+          issue_s(st, b);
         }
       }
-      for (int j = 0; !L::kMerged && ok && j < nb; ++j) {
-        const int st = j % L::kStages, st2 = (j + 1) % L::kStages;
-        if (j + 1 < nb) {
-          const uint32_t ph2 = ((j + 1) / L::kStages) & 1;
-          if (!wait_warp(bar(L::bKFull + st2), ph2, abort_flag, p) ||
-              !wait_warp(bar(L::bVFull + st2), ph2, abort_flag, p) ||
-              !wait_warp(bar(L::bSFree), j & 1, abort_flag, p))
-            break;
-          ptx::tc_fence_after();
-          issue_s(st2);
-        }
-        if (!wait_warp(bar(L::bDSFull), j & 1, abort_flag, p)) break;
-        ptx::tc_fence_after();
-        issue_dq(st, j & 1, j > 0);
-      }
+      if (ok && leader) ptx::mma_commit(bar(L::bGDone));
       if (leader) ptx::mma_commit(bar(L::bDrain));
       wait_drain(bar(L::bDrain), 0, p);
     }
@@ -388,29 +435,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float c = p.c;
     const float2 c2 = make_float2(c, c);
     bool ok = true;
-    for (int j = 0; j < nb; ++j) {
-      const int b = j & 1;
-      if (!wait_warp(bar(L::bSFull), j & 1, abort_flag, p)) { ok = false; break; }
+    if (nb > 0) {
+      // this thread's row of Q (first warpgroup) or dO (second) into TMEM
+      ok = wait_warp(bar(L::bQFull), 0, abort_flag, p);
+      if (ok) {
+        tile_row_to_tmem<D, T>(sm.smem + (h == 0 ? L::kQ : L::kdO), r,
+                               tmem + lane_off + (h == 0 ? L::tQa : L::tdOa));
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::bAFull));
+      }
+    }
+    for (int j = 0; ok && j < nb; ++j) {
+      const int b = j % kBuf;
+      if (!wait_warp(bar(L::bSFull + b), (j / kBuf) & 1, abort_flag, p)) { ok = false; break; }
       ptx::tc_fence_after();
-      // S and dP of this half into registers first, so that the next
-      // block's S and dP products overlap this block's element-wise work
+      const uint32_t cs = tmem + lane_off + L::tS(b) + h * kBwdHalf;
+      const uint32_t cdp = tmem + lane_off + L::tdP(b) + h * kBwdHalf;
       uint32_t s[kBwdHalf], dp[kBwdHalf];
-#pragma unroll
-      for (int cc = 0; cc < kBwdHalf; cc += 32) {
-        ptx::tmem_ld32(tmem + lane_off + L::tS + h * kBwdHalf + cc,
-                       *reinterpret_cast<uint32_t(*)[32]>(&s[cc]));
-        ptx::tmem_ld32(tmem + lane_off + L::tdP + h * kBwdHalf + cc,
-                       *reinterpret_cast<uint32_t(*)[32]>(&dp[cc]));
-      }
+      ptx::tmem_ld32(cs, s);
+      ptx::tmem_ld32(cdp, dp);
       ptx::tmem_wait_ld();
-#pragma unroll
-      for (int cc = 0; cc < kBwdHalf; cc += 32) {
-        ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&s[cc]));
-        ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&dp[cc]));
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(L::bSFree));
-      const int lim = key_lim - j * kBN - h * kBwdHalf;   // this half's columns >= lim: masked
+      ptx::reg_fence32(s);
+      ptx::reg_fence32(dp);
+      const int lim = key_lim - j * kBwdBlk - h * kBwdHalf;   // this half's columns >= lim: masked
       uint32_t pk[kBwdHalf / 2];
       // dS = P .* (dP - D), two columns at a time; the mask test only on
       // blocks where some row of the warp has masked columns
@@ -435,22 +483,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ds_block(std::true_type{});
       else
         ds_block(std::false_type{});
-      if (j >= 2) {
-        // dQ += dS_b K of two blocks back has finished reading dS_b
-        if (!wait_warp(bar(L::bDQDone + b), ((j - 2) >> 1) & 1, abort_flag, p)) { ok = false; break; }
-        ptx::tc_fence_after();
-      }
-      ptx::tmem_st32(tmem + lane_off + L::tdS(b) + h * (kBwdHalf / 2),
-                     *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      // dS over the first 16 columns of this half of dP(b), which only this
+      // thread has read
+      ptx::tmem_st16(cdp, pk);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      // (merged: the MMA thread learns of dS(j) from the next S-read
-      // arrival, so only the last block's dS is announced here)
-      if (!L::kMerged || j == nb - 1) ptx::mbar_arrive(bar(L::bDSFull));
+      ptx::mbar_arrive(bar(L::bDSFull + b));
     }
     // ---- epilogue: dQ = scale * (dS K), this half's columns
-    if (ok && nb > 0)
-      ok = wait_warp(bar(L::bDQDone + ((nb - 1) & 1)), ((nb - 1) >> 1) & 1, abort_flag, p);
+    if (ok && nb > 0) ok = wait_warp(bar(L::bGDone), 0, abort_flag, p);
     if (ok) {
       ptx::tc_fence_after();
       uint16_t *out = reinterpret_cast<uint16_t *>(p.dq) + grow * D + h * (D / 2);
@@ -491,14 +532,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ---------------------------------------------------------------- dK, dV
 template <int D, int T>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,
-                       const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV,
-                       const __grid_constant__ CUtensorMap tmdO,
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ,    // 64-row boxes
+                       const __grid_constant__ CUtensorMap tmK,    // 128-row boxes
+                       const __grid_constant__ CUtensorMap tmV,    // 128-row boxes
+                       const __grid_constant__ CUtensorMap tmdO,   // 64-row boxes
                        const BwdParams p) {
   using L = BwdKVLayout<D, T>;
   using F = typename L::F;
+  using H = typename L::H;
   using E = Elem<T>;
+  constexpr int kBuf = L::kBuf;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const BwdSmem sm = bwd_smem(smem_raw);
   const uint32_t sbase = sm.sbase;
@@ -511,13 +554,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int bh = blockIdx.x / p.n_kblk;
   const int kb = blockIdx.x % p.n_kblk;      // causal: small kb has the most work
   const int k0 = kb * kBN;
-  // query blocks whose rows see at least one of these keys
+  // 64-row query blocks whose rows see at least one of these keys
+  const int n_qb = (p.Nq + kBwdBlk - 1) / kBwdBlk;
   int i_begin = 0;
   if (p.causal) {
     const int first_row = k0 - (p.Nk - p.Nq);     // first row that sees key k0
-    i_begin = first_row > 0 ? first_row / kBM : 0;
+    i_begin = first_row > 0 ? first_row / kBwdBlk : 0;
   }
-  const int nqb = p.n_qblk > i_begin ? p.n_qblk - i_begin : 0;
+  const int nqb = n_qb > i_begin ? n_qb - i_begin : 0;
 
   if (warp == kBwdMmaWarp) {
     ptx::tmem_alloc(sbase + L::kMisc, kTmemCols);
@@ -526,13 +570,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(L::bKVFull), 1);
     for (int s = 0; s < L::kStages; ++s) {
-      ptx::mbar_init(bar(L::bQFull + s), 1);         // Q, dO tiles and LSE, D rows
+      ptx::mbar_init(bar(L::bQFull + s), 1);         // Q, dO blocks and LSE, D rows
       ptx::mbar_init(bar(L::bQEmpty + s), 1);
     }
-    ptx::mbar_init(bar(L::bSFull), 1);
-    ptx::mbar_init(bar(L::bSFree), kBwdEwThreads);
-    ptx::mbar_init(bar(L::bPFull), kBwdEwThreads);
-    ptx::mbar_init(bar(L::bPDone), 1);
+    for (int b = 0; b < kBuf; ++b) {
+      ptx::mbar_init(bar(L::bSFull + b), 1);
+      ptx::mbar_init(bar(L::bPFull + b), kBwdEwThreads);
+    }
+    ptx::mbar_init(bar(L::bAFull), kBwdEwThreads);
+    ptx::mbar_init(bar(L::bGDone), 1);
     ptx::mbar_init(bar(L::bDrain), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -564,17 +610,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (use > 0 && !wait_warp(bar(L::bQEmpty + st), (use - 1) & 1, abort_flag, p)) break;
         const uint32_t sa = sbase + L::stage(st);
         if (leader) {
-          ptx::mbar_arrive_expect_tx(bar(L::bQFull + st), 2 * L::kTile + 2 * kBM * 4);
+          ptx::mbar_arrive_expect_tx(bar(L::bQFull + st), 2 * H::kBytes + 2 * kBwdBlk * 4);
           for (int c = 0; c < F::kChunks; ++c) {
-            ptx::tma_load_3d(sa + c * F::kChunkBytes, &tmQ, bar(L::bQFull + st),
-                             c * F::kChunkElems, i * kBM, bh, pol_q);
-            ptx::tma_load_3d(sa + L::kTile + c * F::kChunkBytes, &tmdO,
-                             bar(L::bQFull + st), c * F::kChunkElems, i * kBM, bh, pol_q);
+            ptx::tma_load_3d(sa + c * H::kChunkBytes, &tmQ, bar(L::bQFull + st),
+                             c * F::kChunkElems, i * kBwdBlk, bh, pol_q);
+            ptx::tma_load_3d(sa + H::kBytes + c * H::kChunkBytes, &tmdO, bar(L::bQFull + st),
+                             c * F::kChunkElems, i * kBwdBlk, bh, pol_q);
           }
-          // the block's 128 rows of LSE (exp2 units) and D: whole padded rows
-          const size_t prow = (size_t)bh * (size_t)p.n_pad + (size_t)i * kBM;
-          ptx::bulk_load(sa + 2 * L::kTile, p.nlse2 + prow, kBM * 4, bar(L::bQFull + st), pol_q);
-          ptx::bulk_load(sa + 2 * L::kTile + kBM * 4, p.ndsum + prow, kBM * 4,
+          // the block's 64 rows of -LSE (exp2 units) and -D: padded rows
+          // (i * 64 + 64 <= n_pad)
+          const size_t prow = (size_t)bh * (size_t)p.n_pad + (size_t)i * kBwdBlk;
+          ptx::bulk_load(sa + 2 * H::kBytes, p.nlse2 + prow, kBwdBlk * 4, bar(L::bQFull + st),
+                         pol_q);
+          ptx::bulk_load(sa + 2 * H::kBytes + kBwdBlk * 4, p.ndsum + prow, kBwdBlk * 4,
                          bar(L::bQFull + st), pol_q);
         }
         issued = n + 1;
@@ -589,102 +637,85 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ================================================= MMA issuer
     if (nqb > 0) {
       const bool leader = ptx::elect_one();
-      constexpr uint32_t idesc_s = make_idesc(kBN, kBM, E::kFmt, false);
+      constexpr uint32_t idesc_s = make_idesc(kBN, kBwdBlk, E::kFmt, false);
       constexpr uint32_t idesc_g = make_idesc(kBN, D, E::kFmt, true);
       const uint64_t dk = make_sdesc(sbase + L::kK, 16, F::kSBO, F::kSwzMode);
       const uint64_t dv = make_sdesc(sbase + L::kV, 16, F::kSBO, F::kSwzMode);
-      // S^T = K Q_st^T and dP^T = V dO_st^T, then a commit on s_full
-      auto issue_s = [&](int st) {
-        const uint32_t sa = sbase + L::stage(st);
-        const uint64_t dq_ = make_sdesc(sa, 16, F::kSBO, F::kSwzMode);
-        const uint64_t ddo = make_sdesc(sa + L::kTile, 16, F::kSBO, F::kSwzMode);
+      const uint64_t dq0 = make_sdesc(sbase + L::stage(0), 16, F::kSBO, F::kSwzMode);
+      const uint64_t ddo0 = make_sdesc(sbase + L::stage(0) + H::kBytes, 16, F::kSBO, F::kSwzMode);
+      const uint64_t dqmn0 = make_sdesc(sbase + L::stage(0), H::kChunkBytes, F::kSBO, F::kSwzMode);
+      const uint64_t ddomn0 = make_sdesc(sbase + L::stage(0) + H::kBytes, H::kChunkBytes, F::kSBO,
+                                         F::kSwzMode);
+      // S^T(b) = K Q_st^T and dP^T(b) = V dO_st^T, then a commit on s_full[b]
+      auto issue_s = [&](int st, int b) {
+        const uint64_t so = (uint64_t)((st * L::kStageBytes) >> 4);
         if (leader) {
-          // all of S^T's steps, then all of dP^T's
 #pragma unroll
           for (int kk = 0; kk < D / E::kMmaK; ++kk) {
-            const uint32_t off = ((kk >> 2) * F::kChunkBytes + (kk & 3) * 32) >> 4;
-            ptx::mma_ss(tmem + L::tS, dk + off, dq_ + off, idesc_s, kk > 0);
+            const uint32_t ob = ((kk >> 2) * H::kChunkBytes + (kk & 3) * 32) >> 4;
+            if constexpr (L::kATmem) {
+              ptx::mma_ts(tmem + L::tS(b), tmem + L::tKa + kk * 8, dq0 + so + ob, idesc_s, kk > 0);
+            } else {
+              const uint32_t oa = ((kk >> 2) * F::kChunkBytes + (kk & 3) * 32) >> 4;
+              ptx::mma_ss(tmem + L::tS(b), dk + oa, dq0 + so + ob, idesc_s, kk > 0);
+            }
           }
 #pragma unroll
           for (int kk = 0; kk < D / E::kMmaK; ++kk) {
-            const uint32_t off = ((kk >> 2) * F::kChunkBytes + (kk & 3) * 32) >> 4;
-            ptx::mma_ss(tmem + L::tdP, dv + off, ddo + off, idesc_s, kk > 0);
+            const uint32_t ob = ((kk >> 2) * H::kChunkBytes + (kk & 3) * 32) >> 4;
+            if constexpr (L::kATmem) {
+              ptx::mma_ts(tmem + L::tdP(b), tmem + L::tVa + kk * 8, ddo0 + so + ob, idesc_s,
+                          kk > 0);
+            } else {
+              const uint32_t oa = ((kk >> 2) * F::kChunkBytes + (kk & 3) * 32) >> 4;
+              ptx::mma_ss(tmem + L::tdP(b), dv + oa, ddo0 + so + ob, idesc_s, kk > 0);
+            }
           }
-          ptx::mma_commit(bar(L::bSFull));
+          ptx::mma_commit(bar(L::bSFull + b));
         }
       };
-      // dV (+)= P^T dO_st and dK (+)= dS^T Q_st, then commits on p_done and
+      // dV (+)= P^T(b) dO_st and dK (+)= dS^T(b) Q_st, then a commit on
       // q_empty[st]
-      auto issue_g = [&](int st, bool acc) {
-        const uint32_t sa = sbase + L::stage(st);
-        const uint64_t dq_mn = make_sdesc(sa, F::kChunkBytes, F::kSBO, F::kSwzMode);
-        const uint64_t ddo_mn = make_sdesc(sa + L::kTile, F::kChunkBytes, F::kSBO, F::kSwzMode);
+      auto issue_g = [&](int st, int b, bool acc) {
+        const uint64_t so = (uint64_t)((st * L::kStageBytes) >> 4);
         if (leader) {
-          // all of dV's steps, then all of dK's (one accumulator at a time)
 #pragma unroll
-          for (int kk = 0; kk < kBM / E::kMmaK; ++kk)
-            ptx::mma_ts(tmem + L::tdV, tmem + L::tP + kk * 8,
-                        ddo_mn + (uint64_t)((kk * E::kMmaK * F::kSwz) >> 4), idesc_g,
+          for (int kk = 0; kk < kBwdBlk / E::kMmaK; ++kk)
+            ptx::mma_ts(tmem + L::tdV, tmem + L::tS(b) + half_cols(kk),
+                        ddomn0 + so + (uint64_t)((kk * E::kMmaK * F::kSwz) >> 4), idesc_g,
                         (acc || kk > 0) ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < kBM / E::kMmaK; ++kk)
-            ptx::mma_ts(tmem + L::tdK, tmem + L::tdS + kk * 8,
-                        dq_mn + (uint64_t)((kk * E::kMmaK * F::kSwz) >> 4), idesc_g,
+          for (int kk = 0; kk < kBwdBlk / E::kMmaK; ++kk)
+            ptx::mma_ts(tmem + L::tdK, tmem + L::tdP(b) + half_cols(kk),
+                        dqmn0 + so + (uint64_t)((kk * E::kMmaK * F::kSwz) >> 4), idesc_g,
                         (acc || kk > 0) ? 1u : 0u);
-          ptx::mma_commit(bar(L::bPDone));
           ptx::mma_commit(bar(L::bQEmpty + st));
         }
       };
       bool ok = wait_warp(bar(L::bKVFull), 0, abort_flag, p) &&
-                wait_warp(bar(L::bQFull), 0, abort_flag, p);
-      if (ok) {
+                (!L::kATmem || wait_warp(bar(L::bAFull), 0, abort_flag, p));
+      for (int n = 0; ok && n < kBuf && n < nqb; ++n) {
+        if (!wait_warp(bar(L::bQFull + n), 0, abort_flag, p)) { ok = false; break; }
         ptx::tc_fence_after();
-        issue_s(0);
+        issue_s(n, n);
       }
-      if constexpr (L::kEarly) {
-        for (int n = 0; ok && n < nqb; ++n) {
-          const int st2 = (n + 1) % L::kStages;
-          if (n + 1 < nqb &&
-              !wait_warp(bar(L::bQFull + st2), ((n + 1) / L::kStages) & 1, abort_flag, p)) {
+      for (int n = 0; ok && n < nqb; ++n) {
+        const int b = n % kBuf;
+        if (!wait_warp(bar(L::bPFull + b), (n / kBuf) & 1, abort_flag, p)) { ok = false; break; }
+        ptx::tc_fence_after();
+        issue_g(n % L::kStages, b, n > 0);
+        const int m = n + kBuf;   // into the buffer just read
+        if (m < nqb) {
+          const int st = m % L::kStages;
+          if (!wait_warp(bar(L::bQFull + st), (m / L::kStages) & 1, abort_flag, p)) {
             ok = false;
             break;
           }
-          // S^T(n), dP^T(n) are in registers; P^T(n-1), dS^T(n-1) were
-          // written before that.  The gradient products of block n-1 go
-          // first: the element-wise warps wait for them before their next
-          // P^T store.
-          if (!wait_warp(bar(L::bSFree), n & 1, abort_flag, p)) { ok = false; break; }
           ptx::tc_fence_after();
-          if (n > 0) issue_g((n - 1) % L::kStages, n > 1);
-          if (n + 1 < nqb) issue_s(st2);
-        }
-        if (ok && wait_warp(bar(L::bPFull), 0, abort_flag, p)) {
-          ptx::tc_fence_after();
-          issue_g((nqb - 1) % L::kStages, nqb > 1);
+          issue_s(st, b);
         }
       }
-      for (int n = 0; !L::kEarly && ok && n < nqb; ++n) {
-        const int st = n % L::kStages, st2 = (n + 1) % L::kStages;
-        const uint32_t ph2 = ((n + 1) / L::kStages) & 1;
-        const bool more = n + 1 < nqb;
-        if (L::kEarly && more) {
-          if (!wait_warp(bar(L::bQFull + st2), ph2, abort_flag, p) ||
-              !wait_warp(bar(L::bSFree), n & 1, abort_flag, p))
-            break;
-          ptx::tc_fence_after();
-          issue_s(st2);
-        }
-        if (!wait_warp(bar(L::bPFull), n & 1, abort_flag, p)) break;
-        ptx::tc_fence_after();
-        issue_g(st, n > 0);
-        if (!L::kEarly && more) {
-          // P^T and dS^T share columns with S^T and dP^T: the next scores go
-          // in only after the gradient MMAs (issue order is execution order)
-          if (!wait_warp(bar(L::bQFull + st2), ph2, abort_flag, p)) break;
-          ptx::tc_fence_after();
-          issue_s(st2);
-        }
-      }
+      if (ok && leader) ptx::mma_commit(bar(L::bGDone));
       if (leader) ptx::mma_commit(bar(L::bDrain));
       wait_drain(bar(L::bDrain), 0, p);
     }
@@ -698,38 +729,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float2 c2 = make_float2(c, c);
     const int shift = p.Nk - p.Nq;                  // causal: key <= row + shift
     bool ok = true;
-    for (int n = 0; n < nqb; ++n) {
+    if constexpr (L::kATmem) {
+      if (nqb > 0) {
+        // this thread's row of K (first warpgroup) or V (second) into TMEM
+        ok = wait_warp(bar(L::bKVFull), 0, abort_flag, p);
+        if (ok) {
+          tile_row_to_tmem<D, T>(sm.smem + (h == 0 ? L::kK : L::kV), r,
+                                 tmem + lane_off + (h == 0 ? L::tKa : L::tVa));
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(L::bAFull));
+        }
+      }
+    }
+    for (int n = 0; ok && n < nqb; ++n) {
       const int i = i_begin + n;
       const int st = n % L::kStages;
-      if (!wait_warp(bar(L::bSFull), n & 1, abort_flag, p) ||
+      const int b = n % kBuf;
+      if (!wait_warp(bar(L::bSFull + b), (n / kBuf) & 1, abort_flag, p) ||
           !wait_warp(bar(L::bQFull + st), (n / L::kStages) & 1, abort_flag, p)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
-      const float *lse_s = reinterpret_cast<const float *>(sm.smem + L::stage(st) + 2 * L::kTile) +
+      const float *lse_s = reinterpret_cast<const float *>(sm.smem + L::stage(st) + 2 * H::kBytes) +
                            h * kBwdHalf;
-      const float *d_s = lse_s + kBM;
+      const float *d_s = lse_s + kBwdBlk;
       // columns (query rows) of this half before `first` do not see the key
-      const int first = p.causal ? key - shift - i * kBM - h * kBwdHalf : 0;
-      // S^T and dP^T of this half into registers first, so that the next
-      // block's products overlap this block's element-wise work
+      const int first = p.causal ? key - shift - i * kBwdBlk - h * kBwdHalf : 0;
+      const uint32_t cs = tmem + lane_off + L::tS(b) + h * kBwdHalf;
+      const uint32_t cdp = tmem + lane_off + L::tdP(b) + h * kBwdHalf;
       uint32_t s[kBwdHalf], dp[kBwdHalf];
-#pragma unroll
-      for (int cc = 0; cc < kBwdHalf; cc += 32) {
-        ptx::tmem_ld32(tmem + lane_off + L::tS + h * kBwdHalf + cc,
-                       *reinterpret_cast<uint32_t(*)[32]>(&s[cc]));
-        ptx::tmem_ld32(tmem + lane_off + L::tdP + h * kBwdHalf + cc,
-                       *reinterpret_cast<uint32_t(*)[32]>(&dp[cc]));
-      }
+      ptx::tmem_ld32(cs, s);
+      ptx::tmem_ld32(cdp, dp);
       ptx::tmem_wait_ld();
-#pragma unroll
-      for (int cc = 0; cc < kBwdHalf; cc += 32) {
-        ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&s[cc]));
-        ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&dp[cc]));
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(L::bSFree));
+      ptx::reg_fence32(s);
+      ptx::reg_fence32(dp);
       uint32_t pkp[kBwdHalf / 2], pkd[kBwdHalf / 2];
       // P^T and dS^T = P^T .* (dP^T - D), two columns at a time (the
       // staged rows hold -LSE in exp2 units and -D); the causal test only on
@@ -767,23 +802,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         p_block(std::true_type{});
       else
         p_block(std::false_type{});
-      if (n > 0) {
-        // the gradient MMAs of the previous block have read P^T and dS^T
-        if (!wait_warp(bar(L::bPDone), (n - 1) & 1, abort_flag, p)) { ok = false; break; }
-        ptx::tc_fence_after();
-      }
-      ptx::tmem_st32(tmem + lane_off + L::tP + h * (kBwdHalf / 2),
-                     *reinterpret_cast<uint32_t(*)[32]>(&pkp[0]));
-      ptx::tmem_st32(tmem + lane_off + L::tdS + h * (kBwdHalf / 2),
-                     *reinterpret_cast<uint32_t(*)[32]>(&pkd[0]));
+      // P^T over the first 16 columns of this half of S^T(b), dS^T over
+      // those of dP^T(b): columns only this thread has read
+      ptx::tmem_st16(cs, pkp);
+      ptx::tmem_st16(cdp, pkd);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      // (early layout: the MMA thread learns of P^T(n) from the next S-read
-      // arrival, so only the last block's is announced here)
-      if (!L::kEarly || n == nqb - 1) ptx::mbar_arrive(bar(L::bPFull));
+      ptx::mbar_arrive(bar(L::bPFull + b));
     }
     // ---- epilogue: dV and dK = scale * (dS^T Q), this half's columns
-    if (ok && nqb > 0) ok = wait_warp(bar(L::bPDone), (nqb - 1) & 1, abort_flag, p);
+    if (ok && nqb > 0) ok = wait_warp(bar(L::bGDone), 0, abort_flag, p);
     if (ok) {
       ptx::tc_fence_after();
       const bool valid = key < p.Nk;
