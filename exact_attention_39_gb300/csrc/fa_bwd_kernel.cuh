@@ -153,6 +153,11 @@ struct BwdQLayout {
   static constexpr int kRing = 2 * kTile;
   static constexpr int kStageBytes = 2 * H::kBytes;      // K block, V block
   static constexpr int kBars = kRing + kStages * kStageBytes;
+  // D = 128: the whole MMA warp executes each MMA, predicated on the issuing
+  // lane (see ptx::mma_ts_if); D = 64: the issuing lane alone, in a branch.
+  // Measured on the GB300 per kernel and head dim: predicated +4 % (dQ) and
+  // +5 % (dK/dV) at D = 128, -4 % and -3 % at D = 64.
+  static constexpr bool kPredIssue = D == 128;
   static constexpr int bQFull = 0;
   static constexpr int bKVFull = 1;                      // [stages]
   static constexpr int bKVEmpty = bKVFull + kStages;     // [stages]
@@ -192,6 +197,7 @@ struct BwdKVLayout {
   static constexpr int kK = 0, kV = kTile;
   static constexpr int kStage0 = 2 * kTile;
   static constexpr int kBars = kStage0 + kStages * kStageBytes;
+  static constexpr bool kPredIssue = D == 128;   // as in the dQ kernel
   static constexpr int bKVFull = 0;
   static constexpr int bQFull = 1;                       // [stages]
   static constexpr int bQEmpty = bQFull + kStages;       // [stages]
@@ -218,6 +224,27 @@ struct BwdKVLayout {
 template <int T>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return T == kBF16 ? ptx::pack_bf16(lo, hi) : ptx::pack_f16(lo, hi);
+}
+
+// MMA issue in one of two forms: kPred, the whole warp executes the
+// instruction predicated on `issue`; otherwise the caller is already inside
+// the issuing lane's branch and the instruction is plain.
+template <bool kPred>
+__device__ __forceinline__ void mma_ts_sel(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t acc, uint32_t issue) {
+  if constexpr (kPred) ptx::mma_ts_if(d, a, b, idesc, acc, issue);
+  else ptx::mma_ts(d, a, b, idesc, acc);
+}
+template <bool kPred>
+__device__ __forceinline__ void mma_ss_sel(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                           uint32_t acc, uint32_t issue) {
+  if constexpr (kPred) ptx::mma_ss_if(d, a, b, idesc, acc, issue);
+  else ptx::mma_ss(d, a, b, idesc, acc);
+}
+template <bool kPred>
+__device__ __forceinline__ void mma_commit_sel(uint32_t bar, uint32_t issue) {
+  if constexpr (kPred) ptx::mma_commit_if(bar, issue);
+  else ptx::mma_commit(bar);
 }
 
 // Shared set-up of both main kernels: 1 KB-aligned shared memory, TMEM
@@ -359,6 +386,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ================================================= MMA issuer
     if (nb > 0) {
       const bool leader = ptx::elect_one();
+      const uint32_t iss = leader ? 1u : 0u;   // the issuing lane (predicated issue)
+      constexpr bool kP = L::kPredIssue;
       constexpr uint32_t idesc_s = make_idesc(kBM, kBwdBlk, E::kFmt, false);
       constexpr uint32_t idesc_q = make_idesc(kBM, D, E::kFmt, true);
       const uint64_t dk0 = make_sdesc(sbase + L::stage(0), 16, F::kSBO, F::kSwzMode);
@@ -367,31 +396,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // S(b) = Q K_st^T and dP(b) = dO V_st^T, then a commit on s_full[b]
       auto issue_s = [&](int st, int b) {
         const uint64_t so = (uint64_t)((st * L::kStageBytes) >> 4);
-        if (leader) {
+        if (kP || leader) {
 #pragma unroll
           for (int kk = 0; kk < D / E::kMmaK; ++kk) {
             const uint32_t off = ((kk >> 2) * H::kChunkBytes + (kk & 3) * 32) >> 4;
-            ptx::mma_ts(tmem + L::tS(b), tmem + L::tQa + kk * 8, dk0 + so + off, idesc_s, kk > 0);
+            mma_ts_sel<kP>(tmem + L::tS(b), tmem + L::tQa + kk * 8, dk0 + so + off, idesc_s,
+                           kk > 0, iss);
           }
 #pragma unroll
           for (int kk = 0; kk < D / E::kMmaK; ++kk) {
             const uint32_t off = ((kk >> 2) * H::kChunkBytes + (kk & 3) * 32) >> 4;
-            ptx::mma_ts(tmem + L::tdP(b), tmem + L::tdOa + kk * 8, dv0 + so + off, idesc_s,
-                        kk > 0);
+            mma_ts_sel<kP>(tmem + L::tdP(b), tmem + L::tdOa + kk * 8, dv0 + so + off, idesc_s,
+                           kk > 0, iss);
           }
-          ptx::mma_commit(bar(L::bSFull + b));
+          mma_commit_sel<kP>(bar(L::bSFull + b), iss);
         }
       };
       // dQ (+)= dS(b) K_st, then a commit on kv_empty[st]
       auto issue_dq = [&](int st, int b, bool acc) {
         const uint64_t so = (uint64_t)((st * L::kStageBytes) >> 4);
-        if (leader) {
+        if (kP || leader) {
 #pragma unroll
           for (int kk = 0; kk < kBwdBlk / E::kMmaK; ++kk)
-            ptx::mma_ts(tmem + L::tdQ, tmem + L::tdP(b) + half_cols(kk),
-                        dkmn0 + so + (uint64_t)((kk * E::kMmaK * F::kSwz) >> 4), idesc_q,
-                        (acc || kk > 0) ? 1u : 0u);
-          ptx::mma_commit(bar(L::bKVEmpty + st));
+            mma_ts_sel<kP>(tmem + L::tdQ, tmem + L::tdP(b) + half_cols(kk),
+                           dkmn0 + so + (uint64_t)((kk * E::kMmaK * F::kSwz) >> 4), idesc_q,
+                           (acc || kk > 0) ? 1u : 0u, iss);
+          mma_commit_sel<kP>(bar(L::bKVEmpty + st), iss);
         }
       };
       bool ok = wait_warp(bar(L::bAFull), 0, abort_flag, p);
@@ -637,6 +667,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ================================================= MMA issuer
     if (nqb > 0) {
       const bool leader = ptx::elect_one();
+      const uint32_t iss = leader ? 1u : 0u;   // the issuing lane (predicated issue)
+      constexpr bool kP = L::kPredIssue;
       constexpr uint32_t idesc_s = make_idesc(kBN, kBwdBlk, E::kFmt, false);
       constexpr uint32_t idesc_g = make_idesc(kBN, D, E::kFmt, true);
       const uint64_t dk = make_sdesc(sbase + L::kK, 16, F::kSBO, F::kSwzMode);
@@ -649,47 +681,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // S^T(b) = K Q_st^T and dP^T(b) = V dO_st^T, then a commit on s_full[b]
       auto issue_s = [&](int st, int b) {
         const uint64_t so = (uint64_t)((st * L::kStageBytes) >> 4);
-        if (leader) {
+        if (kP || leader) {
 #pragma unroll
           for (int kk = 0; kk < D / E::kMmaK; ++kk) {
             const uint32_t ob = ((kk >> 2) * H::kChunkBytes + (kk & 3) * 32) >> 4;
             if constexpr (L::kATmem) {
-              ptx::mma_ts(tmem + L::tS(b), tmem + L::tKa + kk * 8, dq0 + so + ob, idesc_s, kk > 0);
+              mma_ts_sel<kP>(tmem + L::tS(b), tmem + L::tKa + kk * 8, dq0 + so + ob, idesc_s,
+                             kk > 0, iss);
             } else {
               const uint32_t oa = ((kk >> 2) * F::kChunkBytes + (kk & 3) * 32) >> 4;
-              ptx::mma_ss(tmem + L::tS(b), dk + oa, dq0 + so + ob, idesc_s, kk > 0);
+              mma_ss_sel<kP>(tmem + L::tS(b), dk + oa, dq0 + so + ob, idesc_s, kk > 0, iss);
             }
           }
 #pragma unroll
           for (int kk = 0; kk < D / E::kMmaK; ++kk) {
             const uint32_t ob = ((kk >> 2) * H::kChunkBytes + (kk & 3) * 32) >> 4;
             if constexpr (L::kATmem) {
-              ptx::mma_ts(tmem + L::tdP(b), tmem + L::tVa + kk * 8, ddo0 + so + ob, idesc_s,
-                          kk > 0);
+              mma_ts_sel<kP>(tmem + L::tdP(b), tmem + L::tVa + kk * 8, ddo0 + so + ob, idesc_s,
+                             kk > 0, iss);
             } else {
               const uint32_t oa = ((kk >> 2) * F::kChunkBytes + (kk & 3) * 32) >> 4;
-              ptx::mma_ss(tmem + L::tdP(b), dv + oa, ddo0 + so + ob, idesc_s, kk > 0);
+              mma_ss_sel<kP>(tmem + L::tdP(b), dv + oa, ddo0 + so + ob, idesc_s, kk > 0, iss);
             }
           }
-          ptx::mma_commit(bar(L::bSFull + b));
+          mma_commit_sel<kP>(bar(L::bSFull + b), iss);
         }
       };
       // dV (+)= P^T(b) dO_st and dK (+)= dS^T(b) Q_st, then a commit on
       // q_empty[st]
       auto issue_g = [&](int st, int b, bool acc) {
         const uint64_t so = (uint64_t)((st * L::kStageBytes) >> 4);
-        if (leader) {
+        if (kP || leader) {
 #pragma unroll
           for (int kk = 0; kk < kBwdBlk / E::kMmaK; ++kk)
-            ptx::mma_ts(tmem + L::tdV, tmem + L::tS(b) + half_cols(kk),
-                        ddomn0 + so + (uint64_t)((kk * E::kMmaK * F::kSwz) >> 4), idesc_g,
-                        (acc || kk > 0) ? 1u : 0u);
+            mma_ts_sel<kP>(tmem + L::tdV, tmem + L::tS(b) + half_cols(kk),
+                           ddomn0 + so + (uint64_t)((kk * E::kMmaK * F::kSwz) >> 4), idesc_g,
+                           (acc || kk > 0) ? 1u : 0u, iss);
 #pragma unroll
           for (int kk = 0; kk < kBwdBlk / E::kMmaK; ++kk)
-            ptx::mma_ts(tmem + L::tdK, tmem + L::tdP(b) + half_cols(kk),
-                        dqmn0 + so + (uint64_t)((kk * E::kMmaK * F::kSwz) >> 4), idesc_g,
-                        (acc || kk > 0) ? 1u : 0u);
-          ptx::mma_commit(bar(L::bQEmpty + st));
+            mma_ts_sel<kP>(tmem + L::tdK, tmem + L::tdP(b) + half_cols(kk),
+                           dqmn0 + so + (uint64_t)((kk * E::kMmaK * F::kSwz) >> 4), idesc_g,
+                           (acc || kk > 0) ? 1u : 0u, iss);
+          mma_commit_sel<kP>(bar(L::bQEmpty + st), iss);
         }
       };
       bool ok = wait_warp(bar(L::bKVFull), 0, abort_flag, p) &&
