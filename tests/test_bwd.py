@@ -179,6 +179,17 @@ def test_bwd_small_and_ragged(n):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("n", [63, 64, 65, 191, 193])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_inner_block_boundaries(n, causal, d):
+    # both kernels loop over 64-row inner blocks (query blocks in the dK/dV
+    # kernel, key blocks in the dQ kernel): lengths just below, at and above
+    # a multiple of 64, so that the last block is partial, full, or one row
+    run_and_check(W.Workload("bwd_blk", 1, 2, n, d, "bf16", causal, seed=3 * n + d))
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("w", [W.N2048, W.N2048_CAUSAL, W.N8192, W.N8192_CAUSAL],
                          ids=lambda w: w.name)
 def test_bwd_benchmark_shapes_d64(w):
