@@ -26,7 +26,9 @@
 // Both main kernels: warps 0-7 element-wise in two warpgroups (thread = TMEM
 // lane; warpgroup h takes columns 32h .. 32h+31 of each 64-column block and
 // half of the output columns), warp 8 TMA producer, warp 9 TMEM allocator
-// and MMA issuer (the whole warp runs the loop, one elected lane issues).
+// and MMA issuer (the whole warp runs the loop and one elected lane issues:
+// inside a branch of its own at D = 64, as a predicate on MMAs the whole
+// warp executes at D = 128).
 //
 // Pipelining.  S and dP of a block live in one of kBuf TMEM buffers; the
 // MMA thread issues the gradient product of block n and then, into the same

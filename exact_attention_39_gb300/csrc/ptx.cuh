@@ -194,7 +194,7 @@ __device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
-// The same four MMA forms and the commit, executed by a whole warp and issued
+// The 16-bit MMA forms and the commit, executed by a whole warp and issued
 // by the one lane whose `issue` is nonzero.  No branch around the
 // instruction: the warp stays converged, so the vote or wait that follows
 // does not first have to gather a lane that went off alone to issue (about
@@ -217,30 +217,6 @@ __device__ __forceinline__ void mma_ts_if(uint32_t d_tmem, uint32_t a_tmem, uint
       "setp.ne.b32 p, %4, 0;\n\t"
       "setp.ne.b32 q, %5, 0;\n\t"
       "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_ss_f8_if(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate,
-                                             uint32_t issue) {
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "setp.ne.b32 q, %5, 0;\n\t"
-      "@q tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_ts_f8_if(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate,
-                                             uint32_t issue) {
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "setp.ne.b32 q, %5, 0;\n\t"
-      "@q tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
       : "memory");
 }
@@ -295,15 +271,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, "
-      "%7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : FA_O8(r, 0), FA_O8(r, 8)
-      : "r"(taddr)
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_st32(uint32_t taddr,
                                           const uint32_t (&r)[32]) {
   asm volatile(
@@ -327,10 +294,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
 // preceding tmem_wait_ld().
 __device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
   asm volatile("" : FA_F8(r, 0), FA_F8(r, 8), FA_F8(r, 16), FA_F8(r, 24));
-}
-
-__device__ __forceinline__ void reg_fence16(uint32_t *r) {
-  asm volatile("" : FA_F8(r, 0), FA_F8(r, 8));
 }
 
 // Per-warpgroup register budget changes (every warp of the warpgroup
