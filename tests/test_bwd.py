@@ -190,6 +190,35 @@ def test_bwd_inner_block_boundaries(n, causal, d):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_d128_many_blocks(causal):
+    # d = 128 (predicated MMA issue, two S/dP buffers, four-stage rings):
+    # 32 inner blocks per CTA, every row and key of two heads checked
+    run_and_check(W.Workload("bwd_d128", 1, 2, 2048, 128, "bf16", causal, seed=21,
+                             in_mult=0.5))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_deterministic(d):
+    # no atomics and a fixed order of every sum: a second call on the same
+    # inputs gives the same bits (d = 64 and d = 128 issue their MMAs in the
+    # two different forms)
+    w = W.Workload("bwd_det", 2, 3, 777, d, "bf16", True, seed=11 + d)
+    dev = torch.device("cuda")
+    q, k, v = (t.to(dev) for t in W.make_inputs(w))
+    g = W.make_upstream_grad(w).to(dev)
+    o, lse = fa.fwd(q, k, v, causal=w.causal, scale=w.scale)
+    first = fa.bwd(q, k, v, o, lse, g, causal=w.causal, scale=w.scale)
+    second = fa.bwd(q, k, v, o, lse, g, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == 0
+    for a, b_ in zip(first, second):
+        assert torch.equal(a, b_)
+        assert torch.isfinite(a.float()).all()
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("w", [W.N2048, W.N2048_CAUSAL, W.N8192, W.N8192_CAUSAL],
                          ids=lambda w: w.name)
 def test_bwd_benchmark_shapes_d64(w):
