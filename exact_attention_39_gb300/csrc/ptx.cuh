@@ -290,6 +290,41 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
       : "memory");
 }
 
+// 64 consecutive columns of this thread's TMEM lane in one instruction.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t *r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
+      "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, "
+      "%44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, "
+      "%58, %59, %60, %61, %62, %63 "
+      "}, [%64];"
+      : FA_O8(r, 0), FA_O8(r, 8), FA_O8(r, 16), FA_O8(r, 24),
+        FA_O8(r, 32), FA_O8(r, 40), FA_O8(r, 48), FA_O8(r, 56)
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t *r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {"
+      "%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, "
+      "%44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, "
+      "%58, %59, %60, %61, %62, %63, %64 "
+      "};"
+      ::"r"(taddr), FA_I8(r, 0), FA_I8(r, 8), FA_I8(r, 16), FA_I8(r, 24),
+        FA_I8(r, 32), FA_I8(r, 40), FA_I8(r, 48), FA_I8(r, 56)
+      : "memory");
+}
+
+__device__ __forceinline__ void reg_fence64(uint32_t *r) {
+  asm volatile("" : FA_F8(r, 0), FA_F8(r, 8), FA_F8(r, 16), FA_F8(r, 24),
+                    FA_F8(r, 32), FA_F8(r, 40), FA_F8(r, 48), FA_F8(r, 56));
+}
+
 // Keeps the compiler from using registers written by tcgen05.ld before the
 // preceding tmem_wait_ld().
 __device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
