@@ -21,8 +21,8 @@
 //                       dP, dQ += dS K (K read as the MN-major B operand)
 //   fa_bwd_dkdv_kernel  one CTA per 128 keys, looping over 64-row query
 //                       blocks: S^T = K Q^T and dP^T = V dO^T (keys on TMEM
-//                       lanes), P^T over S^T and dS^T over dP^T, dV += P^T dO,
-//                       dK += dS^T Q
+//                       lanes), P^T and dS^T written over S^T (one store),
+//                       dV += P^T dO, dK += dS^T Q
 // Both main kernels: warps 0-7 element-wise in two warpgroups (thread = TMEM
 // lane; warpgroup h takes columns 32h .. 32h+31 of each 64-column block and
 // half of the output columns), warp 8 TMA producer, warp 9 TMEM allocator
@@ -721,7 +721,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                            (acc || kk > 0) ? 1u : 0u, iss);
 #pragma unroll
           for (int kk = 0; kk < kBwdBlk / E::kMmaK; ++kk)
-            mma_ts_sel<kP>(tmem + L::tdK, tmem + L::tdP(b) + half_cols(kk),
+            mma_ts_sel<kP>(tmem + L::tdK, tmem + L::tS(b) + half_cols(kk) + 16,
                            dqmn0 + so + (uint64_t)((kk * E::kMmaK * F::kSwz) >> 4), idesc_g,
                            (acc || kk > 0) ? 1u : 0u, iss);
           mma_commit_sel<kP>(bar(L::bQEmpty + st), iss);
@@ -800,7 +800,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::tmem_wait_ld();
       ptx::reg_fence32(s);
       ptx::reg_fence32(dp);
-      uint32_t pkp[kBwdHalf / 2], pkd[kBwdHalf / 2];
+      // P^T pairs in pk[0, 16), dS^T pairs in pk[16, 32): one 32-column store
+      uint32_t pk[kBwdHalf];
+      uint32_t *pkp = pk, *pkd = pk + kBwdHalf / 2;
       // P^T and dS^T = P^T .* (dP^T - D), two columns at a time (the
       // staged rows hold -LSE in exp2 units and -D); the causal test only on
       // blocks where some key of the warp has masked columns
@@ -837,10 +839,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         p_block(std::true_type{});
       else
         p_block(std::false_type{});
-      // P^T over the first 16 columns of this half of S^T(b), dS^T over
-      // those of dP^T(b): columns only this thread has read
-      ptx::tmem_st16(cs, pkp);
-      ptx::tmem_st16(cdp, pkd);
+      // P^T over the first 16 columns of this half of S^T(b) and dS^T over
+      // the next 16: columns only this thread has read
+      ptx::tmem_st32(cs, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(L::bPFull + b));
