@@ -81,6 +81,8 @@ constexpr int kRowsPerCta = kBM * kNumQ;
 // much (log2 units): probabilities then stay below 2^8, which fp16, bf16 and
 // the fp32 accumulators hold exactly as well as values below 1.
 constexpr float kRescaleThreshold = 8.0f;
+// Heads per group in the causal work order (see fa_fwd_kernel).
+constexpr int kCausalHeadGroup = 32;
 
 enum : unsigned { kStatusTimeout = 1u };
 
@@ -280,14 +282,19 @@ __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks
 
   // ---- work unit: (head bh, unit of Q * 128 query rows).  Non-causal: the
   // units of a head are consecutive, so the CTAs resident at one time share
-  // K/V blocks in L2.  Causal: units differ in length, so the grid runs the
-  // longest unit of every head first, then the next longest, and so on
-  // (longest-processing-time order keeps the tail short).
+  // K/V blocks in L2.  Causal: units differ in length, so the grid runs, in
+  // groups of kCausalHeadGroup heads, the longest unit of every head of the
+  // group first, then the next longest, and so on (longest-processing-time
+  // order keeps the tail short; a group's K and V, 64 MB at 8192 keys and
+  // d = 64, stay in L2 while it runs).
   int bh, unit;
   if (p.causal) {
     const int nbh = (int)(gridDim.x / (unsigned)p.n_units);
-    bh = (int)(blockIdx.x % (unsigned)nbh);
-    unit = p.n_units - 1 - (int)(blockIdx.x / (unsigned)nbh);
+    const int per_group = kCausalHeadGroup * p.n_units;
+    const int g = (int)blockIdx.x / per_group, r = (int)blockIdx.x % per_group;
+    const int heads = min(kCausalHeadGroup, nbh - g * kCausalHeadGroup);
+    bh = g * kCausalHeadGroup + r % heads;
+    unit = p.n_units - 1 - r / heads;
   } else {
     bh = (int)(blockIdx.x / (unsigned)p.n_units);
     unit = (int)(blockIdx.x % (unsigned)p.n_units);
