@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -197,6 +198,11 @@ fa_status run_shape(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensor
   const long long units = ((long long)p.Nq + Q * kBM - 1) / (Q * kBM);
   if (bh * units > (1ll << 31) - 1) return FA_ERR_SHAPE;
   p.n_units = (int)units;
+  // causal work order: heads per group, from the bytes of one head's K and V
+  const long long kv_head = 2ll * p.Nk * D * Elem<T>::kBytes;
+  long long group = kv_head > 0 ? kCausalGroupKVBytes / kv_head : kCausalMaxHeadGroup;
+  group = std::min<long long>(std::max<long long>(group, 1), kCausalMaxHeadGroup);
+  p.head_group = (int)std::min<long long>(group, bh);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(bh * units), 1, 1);
   cfg.blockDim = dim3(CtaShape<Q>::kThreads, 1, 1);

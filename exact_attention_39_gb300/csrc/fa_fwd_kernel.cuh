@@ -81,8 +81,11 @@ constexpr int kRowsPerCta = kBM * kNumQ;
 // much (log2 units): probabilities then stay below 2^8, which fp16, bf16 and
 // the fp32 accumulators hold exactly as well as values below 1.
 constexpr float kRescaleThreshold = 8.0f;
-// Heads per group in the causal work order (see fa_fwd_kernel).
-constexpr int kCausalHeadGroup = 32;
+// Causal work order: a group of heads holds at most this many bytes of K and
+// V (so that they stay in the 129 MB L2 beside Q and O) and at most
+// kCausalMaxHeadGroup heads.
+constexpr long long kCausalGroupKVBytes = 64ll << 20;
+constexpr int kCausalMaxHeadGroup = 32;
 
 enum : unsigned { kStatusTimeout = 1u };
 
@@ -91,6 +94,7 @@ struct FwdParams {
   float *lse;         // [BH, Nq] output
   int Nq, Nk;         // query and key rows per head
   int n_units;        // work units per head: ceil(Nq / 256)
+  int head_group;     // causal work order: heads per group (see fa_fwd_kernel)
   int causal;
   float c;            // scale * log2(e) (* q and k descales for e4m3), > 0
   float o_scale;      // multiplies O before the division by l (v descale)
@@ -283,17 +287,18 @@ __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks
   // ---- work unit: (head bh, unit of Q * 128 query rows).  Non-causal: the
   // units of a head are consecutive, so the CTAs resident at one time share
   // K/V blocks in L2.  Causal: units differ in length, so the grid runs, in
-  // groups of kCausalHeadGroup heads, the longest unit of every head of the
+  // groups of p.head_group heads, the longest unit of every head of the
   // group first, then the next longest, and so on (longest-processing-time
-  // order keeps the tail short; a group's K and V, 64 MB at 8192 keys and
-  // d = 64, stay in L2 while it runs).
+  // order keeps the tail short; the host sizes a group so that its K and V
+  // stay in L2 while it runs).
   int bh, unit;
   if (p.causal) {
     const int nbh = (int)(gridDim.x / (unsigned)p.n_units);
-    const int per_group = kCausalHeadGroup * p.n_units;
+    const int G = p.head_group;
+    const int per_group = G * p.n_units;
     const int g = (int)blockIdx.x / per_group, r = (int)blockIdx.x % per_group;
-    const int heads = min(kCausalHeadGroup, nbh - g * kCausalHeadGroup);
-    bh = g * kCausalHeadGroup + r % heads;
+    const int heads = min(G, nbh - g * G);
+    bh = g * G + r % heads;
     unit = p.n_units - 1 - r / heads;
   } else {
     bh = (int)(blockIdx.x / (unsigned)p.n_units);
