@@ -545,12 +545,12 @@ __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks
   } else {
     // ================================================= softmax warpgroups
     ptx::regs_inc<C::kRegsSoftmax>();
-    // The non-causal two-tile kernel for 16-bit inputs at D = 64 loads S
-    // and stores P 64 columns an instruction (measured on the GB300: +1.5 to
-    // +2.4 % at N = 2048..8192); the other instantiations keep 32-column
-    // loads and stores, which measured faster for them (causal -3 %, e4m3
-    // -1 % with the wide forms).
-    constexpr bool kWideLdSt = D == 64 && !kF8 && Q == 2 && !kSkip && L::kPCols == 64;
+    // The two-tile kernels for 16-bit inputs at D = 64 load S and store P
+    // 64 columns an instruction (measured on the GB300: +1.5 to +2.4 %
+    // non-causal and +1.0 to +1.2 % causal at N = 2048..8192); the e4m3 and
+    // D = 128 instantiations keep 32-column loads and stores, which measured
+    // faster for them (e4m3 -1 % with the wide forms).
+    constexpr bool kWideLdSt = D == 64 && !kF8 && Q == 2 && L::kPCols == 64;
     const int i = warp >> 2;                  // query tile of this warpgroup
     const int r = threadIdx.x & 127;          // row within the tile = TMEM lane
     const int row = q0 + i * kBM + r;         // query row within the head
