@@ -37,15 +37,17 @@ void *kernel_ptr() {
 }
 
 // Key lengths up to which D = 64 runs one query tile per CTA, two CTAs per
-// SM (CtaShape<1>): with few key blocks per CTA, overlapping one CTA's
-// set-up and epilogue with the other's work pays (measured at B8 H32 N512:
-// +12 % bf16, +18 % fp16); from eight blocks on the two-tile CTA is faster
-// (N1024: -4 %, N2048: -11 % with one tile).  Causal units are shorter on
-// average (half the blocks), so the one-tile shape pays up to twice the keys
-// (B8 H32 N1024 causal: +12 % together with the longest-first order; N2048
-// causal: -7 %).
-constexpr int kOneTileMaxNk = 512;
-constexpr int kOneTileMaxNkCausal = 1024;
+// SM (CtaShape<1>), for 16-bit inputs.  Two resident CTAs overlap one's
+// set-up, first loads, epilogue and exit with the other's key blocks, which a
+// lone two-tile CTA leaves the SM idle for (about 5000 cycles a CTA, measured
+// with a clock64 trace); in steady state the two-tile CTA's key block is
+// about 7 % cheaper per query tile.  Measured against the two-tile shape at
+// B8 H32 d64 bf16: N512 +10 %, N1024 +7 %, N2048 +5 %, N4096 +0.5 %
+// (causal N2048 +3.5 %, N4096 +1 %), N8192 -3.5 % (causal -2 %).  e4m3
+// inputs halve the tensor time of a block, so the overlap pays at every
+// length (N4096 +6 %, N8192 +3 %, causal N8192 +4 %): they always take one
+// tile.
+constexpr int kOneTileMaxNk = 4096;
 
 // One-time, per-process and per-device set-up: the CUDA driver's
 // tensor-map encoder, the kernels' shared-memory opt-in, the status word's address.
@@ -67,31 +69,28 @@ fa_status ensure_ready(int dev) {
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return FA_ERR_CUDA;
   if (major != 10 || minor != 3) return FA_ERR_CUDA;   // built for sm_103a only
-  const void *kernels[9] = {kernel_ptr<64, kF16>(), kernel_ptr<64, kBF16>(),
-                            kernel_ptr<64, kE4M3>(), kernel_ptr<128, kF16>(),
-                            kernel_ptr<128, kBF16>(), kernel_ptr<128, kE4M3>(),
-                            kernel_ptr<64, kF16, 1>(), kernel_ptr<64, kBF16, 1>(),
-                            kernel_ptr<64, kE4M3, 1>()};
-  const int smem[9] = {Layout<64, kF16>::kAlloc, Layout<64, kBF16>::kAlloc,
-                       Layout<64, kE4M3>::kAlloc, Layout<128, kF16>::kAlloc,
-                       Layout<128, kBF16>::kAlloc, Layout<128, kE4M3>::kAlloc,
-                       Layout<64, kF16, 1>::kAlloc, Layout<64, kBF16, 1>::kAlloc,
-                       Layout<64, kE4M3, 1>::kAlloc};
-  for (int t = 0; t < 9; ++t) {
-    if (cudaFuncSetAttribute(kernels[t], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem[t]) != cudaSuccess)
+  // Every forward instantiation the host launches, its shared memory, and
+  // whether two of its CTAs share an SM (the one-tile shape, which needs the
+  // whole carveout as shared memory).  The causal two-tile d = 64 kernels
+  // (last argument true) skip tile 0's block past its diagonal.
+  struct FwdKernel { const void *fn; int smem; bool two_per_sm; };
+  const FwdKernel fwd_kernels[] = {
+      {kernel_ptr<64, kF16>(), Layout<64, kF16>::kAlloc, false},
+      {kernel_ptr<64, kBF16>(), Layout<64, kBF16>::kAlloc, false},
+      {kernel_ptr<64, kF16, 2, true>(), Layout<64, kF16>::kAlloc, false},
+      {kernel_ptr<64, kBF16, 2, true>(), Layout<64, kBF16>::kAlloc, false},
+      {kernel_ptr<128, kF16>(), Layout<128, kF16>::kAlloc, false},
+      {kernel_ptr<128, kBF16>(), Layout<128, kBF16>::kAlloc, false},
+      {kernel_ptr<128, kE4M3>(), Layout<128, kE4M3>::kAlloc, false},
+      {kernel_ptr<64, kF16, 1>(), Layout<64, kF16, 1>::kAlloc, true},
+      {kernel_ptr<64, kBF16, 1>(), Layout<64, kBF16, 1>::kAlloc, true},
+      {kernel_ptr<64, kE4M3, 1>(), Layout<64, kE4M3, 1>::kAlloc, true}};
+  for (const FwdKernel &k : fwd_kernels) {
+    if (cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem) !=
+        cudaSuccess)
       return FA_ERR_CUDA;
-    // the causal two-tile d = 64 instantiations that skip tile 0's last block
-    if (t < 3 && cudaFuncSetAttribute(t == 0   ? kernel_ptr<64, kF16, 2, true>()
-                                      : t == 1 ? kernel_ptr<64, kBF16, 2, true>()
-                                               : kernel_ptr<64, kE4M3, 2, true>(),
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      smem[t]) != cudaSuccess)
-      return FA_ERR_CUDA;
-    // the one-tile shape needs room for two CTAs' shared memory per SM
-    if (t >= 6 && cudaFuncSetAttribute(kernels[t],
-                                       cudaFuncAttributePreferredSharedMemoryCarveout,
-                                       100) != cudaSuccess)
+    if (k.two_per_sm && cudaFuncSetAttribute(k.fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             100) != cudaSuccess)
       return FA_ERR_CUDA;
   }
   const void *bwd_kernels[8] = {
@@ -228,10 +227,13 @@ fa_status run(const void *q, const void *k, const void *v, FwdParams p,
   if (!encode_map<D, T>(&mq, q, p.Nq, bh) || !encode_map<D, T>(&mk, kb, nk_map, bh) ||
       !encode_map<D, T>(&mv, vb, nk_map, bh))
     return FA_ERR_CUDA;
-  if constexpr (D == 64)
-    if (p.Nk <= kOneTileMaxNk || (p.causal && p.Nk <= kOneTileMaxNkCausal))
-      return run_shape<D, T, 1>(mq, mk, mv, p, bh, stream);
-  return run_shape<D, T, 2>(mq, mk, mv, p, bh, stream);
+  if constexpr (D == 64 && Elem<T>::kF8) {
+    return run_shape<D, T, 1>(mq, mk, mv, p, bh, stream);
+  } else {
+    if constexpr (D == 64)
+      if (p.Nk <= kOneTileMaxNk) return run_shape<D, T, 1>(mq, mk, mv, p, bh, stream);
+    return run_shape<D, T, 2>(mq, mk, mv, p, bh, stream);
+  }
 }
 
 bool aligned(const void *p, uintptr_t a);

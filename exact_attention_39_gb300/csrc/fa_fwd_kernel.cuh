@@ -148,8 +148,14 @@ struct Layout {
   static constexpr int bQFull = 0;
   static constexpr int bKFull = 1;
   static constexpr int bVFull = bKFull + kStages;
-  static constexpr int bKVEmpty = bVFull + kStages;
-  static constexpr int bSFull = bKVEmpty + kStages;   // S_i ready (MMA commit)
+  static constexpr int bKVEmpty = bVFull + kStages;  // K and V (K alone when split)
+  // One query tile: K and V of a stage land and free on barriers of their
+  // own, so that K_{j+2} is loaded as soon as the scores of block j are done
+  // instead of after O += P V_j (with two stages the ring could not refill
+  // within one block; the next scores waited for their K).
+  static constexpr bool kSplitKV = Q == 1;
+  static constexpr int bVEmpty = bKVEmpty + kStages;  // V (split only)
+  static constexpr int bSFull = bVEmpty + (kSplitKV ? kStages : 0);   // S_i ready (MMA commit)
   static constexpr int bSFree = bSFull + Q;          // S_i read into registers
   static constexpr int bPFull = bSFree + Q;           // P_i written, O_i rescaled
   static constexpr int bODone = bPFull + Q;           // O_i += P_i V_j done (commit)
@@ -327,6 +333,7 @@ __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks
       ptx::mbar_init(bar(L::bKFull + s), 1);   // K, or K and V when merged
       ptx::mbar_init(bar(L::bVFull + s), 1);
       ptx::mbar_init(bar(L::bKVEmpty + s), 1);
+      if (L::kSplitKV) ptx::mbar_init(bar(L::bVEmpty + s), 1);
     }
     for (int i = 0; i < kNumQ; ++i) {
       ptx::mbar_init(bar(L::bSFull + i), 1);
@@ -367,6 +374,44 @@ __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks
             ptx::tma_load_3d(sbase + L::kQ + i * L::kTileBytes + c * L::kChunkBytes,
                              &tmQ, bar(L::bQFull), c * L::kChunkElems, q0 + i * kBM, bh, pol_q);
       }
+      if constexpr (L::kSplitKV) {
+        // K_{j+1} ahead of V_j: a K stage frees when its scores are done, a
+        // V stage when its product is.
+        auto load = [&](int j, bool is_v) -> bool {
+          const int st = j % L::kStages;
+          const int use = j / L::kStages;
+          const int empty = is_v ? L::bVEmpty : L::bKVEmpty;
+          const int full = is_v ? L::bVFull : L::bKFull;
+          if (use > 0 && !wait_warp(bar(empty + st), (use - 1) & 1, abort_flag, p))
+            return false;
+          if (leader) {
+            ptx::mbar_arrive_expect_tx(bar(full + st), L::kTileBytes);
+            for (int c = 0; c < L::kChunks; ++c)
+              ptx::tma_load_3d(sbase + (is_v ? L::kV : L::kK) + st * L::kTileBytes +
+                                   c * L::kChunkBytes,
+                               is_v ? &tmV : &tmK, bar(full + st), c * L::kChunkElems,
+                               j * kBN, bh, pol_kv);
+          }
+          return true;
+        };
+        int k_issued = 0, v_issued = 0;
+        if (load(0, false)) {
+          k_issued = 1;
+          for (int j = 0; j < nb; ++j) {
+            if (j + 1 < nb) {
+              if (!load(j + 1, false)) break;
+              k_issued = j + 2;
+            }
+            if (!load(j, true)) break;
+            v_issued = j + 1;
+          }
+        }
+        wait_drain(bar(L::bQFull), 0, p);
+        for (int j = max(k_issued - L::kStages, 0); j < k_issued; ++j)
+          wait_drain(bar(L::bKFull + j % L::kStages), (uint32_t)(j / L::kStages) & 1u, p);
+        for (int j = max(v_issued - L::kStages, 0); j < v_issued; ++j)
+          wait_drain(bar(L::bVFull + j % L::kStages), (uint32_t)(j / L::kStages) & 1u, p);
+      } else {
       int issued = 0;
       for (int j = 0; j < nb; ++j) {
         const int st = j % L::kStages;
@@ -397,6 +442,7 @@ __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks
         const uint32_t ph = (uint32_t)(j / L::kStages) & 1u;
         wait_drain(bar(L::bKFull + st), ph, p);
         if (!L::kMerged) wait_drain(bar(L::bVFull + st), ph, p);
+      }
       }
     }
   } else if (warp == kMmaWarp) {
@@ -481,6 +527,7 @@ __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks
       if (ok) {
         ptx::tc_fence_after();
         for (int i = 0; i < kNumQ; ++i) issue_s(i, 0);
+        if (L::kSplitKV && leader) ptx::mma_commit(bar(L::bKVEmpty + 0));
       }
       if constexpr (L::kMerged) {
         for (int j = 0; ok && j < nb; ++j) {
@@ -494,12 +541,16 @@ __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks
               break;
             ptx::tc_fence_after();
             for (int i = 0; i < kNumQ; ++i) issue_s(i, st2);
+            if (L::kSplitKV && leader) ptx::mma_commit(bar(L::bKVEmpty + st2));
           }
-          // V_j landed with K_j; both warpgroups have written P(j)
+          // both warpgroups have written P(j); V_j landed (with K_j unless split)
           if (!wait_warp(bar(L::bPFull), j & 1, abort_flag, p)) break;
+          if (L::kSplitKV &&
+              !wait_warp(bar(L::bVFull + st), (j / L::kStages) & 1, abort_flag, p))
+            break;
           ptx::tc_fence_after();
           for (int i = 0; i < kNumQ; ++i) issue_pv(i, st, j > 0);
-          if (leader) ptx::mma_commit(bar(L::bKVEmpty + st));
+          if (leader) ptx::mma_commit(bar(L::kSplitKV ? L::bVEmpty + st : L::bKVEmpty + st));
         }
       } else {
         for (int j = 0; ok && j < nb; ++j) {

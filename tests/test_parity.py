@@ -111,7 +111,9 @@ def test_sequence_sweep(n, causal):
 
 
 # ------------------------------------------------------------ ragged and small
-# 511..513 straddle the switch between one and two query tiles per CTA
+# 16-bit inputs at d = 64 with at most 4096 keys run one query tile per CTA,
+# K and V on separate ring barriers; 640 and 1000 keys wrap the two-stage
+# ring several times.
 @pytest.mark.parametrize("n", [1, 2, 3, 64, 127, 128, 129, 255, 256, 257, 300, 511, 512, 513,
                                640, 1000])
 @pytest.mark.parametrize("causal", [False, True])
@@ -121,12 +123,26 @@ def test_ragged_lengths_d64(n, causal):
         full_check(w)
 
 
-# Causal problems with more than 1024 keys run the two-tile shape in which the
+# Above 4096 keys 16-bit inputs at d = 64 run two query tiles per CTA.  Short
+# query lengths against 4095..5000 keys straddle the switch and reach the
+# two-tile kernel with ragged query and key tails at sizes the oracle
+# finishes quickly.
+@pytest.mark.parametrize("nq,nk", [(300, 4095), (300, 4096), (300, 4097), (1, 4353),
+                                   (127, 4200), (129, 4200), (256, 4224), (257, 4500),
+                                   (511, 4097), (513, 5000), (1000, 4300)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_shape_switch_and_two_tile_d64(nq, nk, causal):
+    for dtype in ("fp16", "bf16"):
+        w = W.Workload("two_tile", 1, 2, nq, 64, dtype, causal, seed=nq + 3 * nk, Nk=nk)
+        full_check(w)
+
+
+# Causal problems with more than 4096 keys run the two-tile shape in which the
 # first tile skips a key block wholly past its diagonal; ragged lengths and
 # Nq != Nk move that block's position and the first tile's block count.
-@pytest.mark.parametrize("nq,nk", [(1025, 1025), (1100, 1100), (1281, 1281), (1500, 1500),
-                                   (2047, 2047), (2100, 2100), (1300, 1500), (1500, 1300),
-                                   (700, 1200), (1200, 1100), (260, 2049)])
+@pytest.mark.parametrize("nq,nk", [(4097, 4097), (4200, 4200), (4353, 4353), (4500, 4500),
+                                   (5119, 5119), (4300, 4500), (4500, 4300), (700, 4200),
+                                   (4400, 4300), (260, 4353)])
 def test_causal_tile_skip_lengths(nq, nk):
     for dtype in ("fp16", "bf16"):
         w = W.Workload("skip", 1, 3, nq, 64, dtype, True, seed=nq + 7 * nk, Nk=nk)
