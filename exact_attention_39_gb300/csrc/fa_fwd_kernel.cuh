@@ -757,12 +757,24 @@ __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks
 
     // ---- epilogue: O / l and LSE
     if (ok && nb_i > 0) ok = wait_phase(bar(L::bODone + i), (nb_i - 1) & 1, abort_flag, p);
+    // One query tile: each warp stages its 32 rows of O in the tile's Q region
+    // (free once the tile's MMAs are done: the last product's commit covers
+    // every earlier MMA), XOR-swizzled by row so that neither the row-wise
+    // writes nor the chunk-wise reads conflict on banks, then stores them 512
+    // contiguous bytes an instruction instead of 16 bytes to each of 32 rows
+    // (measured: +2 to +4.5 % at N = 512..2048; in the two-tile kernels the
+    // same code cost 5 % at N = 8192 through the main loop's code generation).
+    constexpr bool kStageO = Q == 1;
+    constexpr int kORowBytes = D * 2;
+    static_assert(!kStageO || 128 * kORowBytes <= L::kBars, "staged O fits below the barriers");
+    if constexpr (kStageO) ok = __all_sync(0xffffffffu, ok);   // the staged store is warp-wide
     if (ok) {
       ptx::tc_fence_after();
       const bool valid = row < p.Nq;
       const float inv = l > 0.f ? p.o_scale / l : 0.f;
       const size_t orow = (size_t)bh * (size_t)p.Nq + (size_t)row;
       uint16_t *optr = reinterpret_cast<uint16_t *>(p.o) + orow * D;
+      uint8_t *stage = smem + L::kQ + (warp & 3) * 32 * kORowBytes;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -781,11 +793,32 @@ __global__ void __launch_bounds__(CtaShape<Q>::kThreads, CtaShape<Q>::kMinBlocks
           const float b = __uint_as_float(o[2 * t + 1]) * inv;
           w[t] = kOutBF16 ? ptx::pack_bf16(a, b) : ptx::pack_f16(a, b);
         }
-        if (valid) {
+        if constexpr (kStageO) {
+          uint8_t *srow = stage + lane * kORowBytes;
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            *reinterpret_cast<uint4 *>(srow + (((cc * 4 + t) ^ (lane & 7)) * 16)) =
+                make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+        } else if (valid) {
           uint4 *dst = reinterpret_cast<uint4 *>(optr + cc * 32);
 #pragma unroll
           for (int t = 0; t < 4; ++t)
             dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+        }
+      }
+      if constexpr (kStageO) {
+        __syncwarp();
+        constexpr int kChunksRow = kORowBytes / 16;
+        const int row0 = q0 + (warp & 3) * 32;   // this warp's first row
+        uint4 *obase = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.o) +
+                                                 ((size_t)bh * (size_t)p.Nq + (size_t)row0) * D);
+#pragma unroll
+        for (int k = 0; k < kChunksRow; ++k) {
+          const int idx = k * 32 + lane;   // 16-byte chunk of the warp's rows
+          const int rr = idx / kChunksRow, c = idx % kChunksRow;
+          if (row0 + rr < p.Nq)
+            obase[idx] = *reinterpret_cast<const uint4 *>(stage + rr * kORowBytes +
+                                                          ((c ^ (rr & 7)) * 16));
         }
       }
       if (valid)
