@@ -54,9 +54,10 @@ constexpr int kBN = 128;                 // keys per block
 constexpr int kTmemCols = 512;           // TMEM columns of an SM
 
 // Shape of a CTA with Q query tiles (Q softmax warpgroups and one control
-// warpgroup).  Q = 2 is the default: one CTA per SM.  Q = 1 (D = 64, short
-// query lengths) halves shared memory and TMEM so that two CTAs share an SM
-// and one CTA's set-up and epilogue overlap the other's work.
+// warpgroup).  Q = 2 is the default: one CTA per SM.  Q = 1 (D = 64: 16-bit
+// inputs with at most 4096 keys, and every e4m3 launch) halves shared memory
+// and TMEM so that two CTAs share an SM and one CTA's set-up, first loads,
+// epilogue and exit overlap the other's key blocks.
 template <int Q>
 struct CtaShape {
   static constexpr int kThreads = 128 * Q + 128;

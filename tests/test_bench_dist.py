@@ -66,6 +66,14 @@ def test_kernel_hash_is_stable():
     assert len(bench.kernel_source_hash()) == 16
 
 
+def test_code_digest_ignores_comments_only():
+    src = "int f(int x) {\n  return x + 1;   // one more\n}\n"
+    assert bench.code_digest([src]) == bench.code_digest(
+        ["// header\nint f(int x) {\n\n  return x + 1;   // one more, reworded\n}\n"])
+    assert bench.code_digest([src]) != bench.code_digest([src.replace("x + 1", "x + 2")])
+    assert bench.code_digest([src, ""]) != bench.code_digest(["", src + "int g;"])
+
+
 def test_reference_cli_prints_one_contract_line():
     # the whole command line, as the harness launches it: one JSON line on
     # stdout with the contract's keys (the reference arm runs on CPU)
