@@ -93,6 +93,19 @@ def test_fp8_query_key_lengths(nq, nk):
     check_fp8(w, o, lse, q, k, v, rows=list(range(dead, nq)))
 
 
+# e4m3 at d = 64 runs one query tile per CTA at every length: ragged query and
+# key tails above 4096 keys, where 16-bit inputs switch to two tiles per CTA
+@pytest.mark.gpu
+@pytest.mark.parametrize("nq,nk,causal", [(300, 5000, False), (300, 5000, True),
+                                          (4353, 4353, True), (1, 4200, False)])
+def test_fp8_one_tile_long_keys(nq, nk, causal):
+    w = W.Workload("fp8long", 1, 2, nq, 64, "e4m3", causal, seed=nq + nk, Nk=nk)
+    q, k, v = W.make_inputs(w)
+    o, lse = run_fp8(w, q, k, v)
+    dead = max(0, nq - nk) if causal else 0
+    check_fp8(w, o, lse, q, k, v, rows=list(range(dead, nq)))
+
+
 @pytest.mark.gpu
 def test_fp8_large_logits():
     # logits eight times larger, through the softmax scale (multiplying Q by
