@@ -236,7 +236,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
   }
 }
 
-// wait_phase executed by all 32 lanes of a warp, with one warp-wide verdict.
+// wait_phase executed by all 32 lanes of a warp, with one warp-wide result.
 template <class P>
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity,
                                           volatile int *abort_flag,
