@@ -277,6 +277,9 @@ def time_launches(step, n_sets, warmup, steps, stream, local):
     then ``steps`` times, each bracketed by CUDA events on ``stream``, while
     nvidia-smi samples the clocks.  ``i`` cycles over ``n_sets`` input sets.
     Returns (region ms, per-launch ms list, clock summary)."""
+    # inputs and outputs were made on the device's current stream: the
+    # launches on ``stream`` come after that work
+    stream.wait_stream(torch.cuda.current_stream(stream.device))
     for i in range(warmup):
         step(i % n_sets)
     stream.synchronize()

@@ -270,6 +270,7 @@ def test_deterministic_and_stream_ordered():
     w = W.N2048_CAUSAL.with_(B=2)
     q, k, v = (t.cuda() for t in W.make_inputs(w))
     s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())   # the inputs' copies come first
     with torch.cuda.stream(s):
         o1, l1 = fa.fwd(q, k, v, causal=True, stream=s)
         o2, l2 = fa.fwd(q, k, v, causal=True, stream=s)
